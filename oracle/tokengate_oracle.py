@@ -1,0 +1,243 @@
+"""CPU oracle for the TokenGate gated-prefill path.
+
+TEST INFRASTRUCTURE ONLY. This module is the plain, slow, obviously correct
+definition that the CUDA path is checked against. Only the test suite, the
+package's smoke check and the benchmark's CPU-baseline leg may import it; the
+product path never calls it and shares no code with it.
+
+Arithmetic is numpy float64 throughout. Inputs arrive as float arrays holding
+the exact bf16 (or fp32) values the GPU reads; nothing here rounds to bf16.
+
+Sources (the pages this follows, cited by page and equation):
+  * "TokenGate: Learnable Token Pruning for Fast, Memory-Efficient LLM Prefill",
+    paper deep dive (agientry.com), section 2 Eq. (2); section 3.1 Eqs. (3)-(4);
+    section 3.2 Eqs. (5)-(8); section 3.4 "How the released code implements the
+    paper" (the prune path: score, clamp the budget, select, keep indices, slice
+    the hidden states, gather the original position ids).
+  * "TokenGate" paper page (thelatestinai.com), Figure 1 (b)-(c): the gate keeps
+    K tokens and forwards the kept hidden states with their importance scores;
+    token-gated attention multiplies each attention weight by its key's gate
+    value.
+
+Readings where the pages leave a step open (each is listed in the design notes):
+  * the score MLP is d -> d_g -> 1 with SiLU, and the gate value is
+    g = sigmoid(s); instruction tokens get g = 1 (zero log-bias);
+  * top-K ranks the fp32 pre-sigmoid score s, ties go to the lower index, -0.0
+    ranks as +0.0 and NaN ranks below every number;
+  * attention logit = tau_h * q.k / sqrt(d_h) + beta_h * ln g_j, with
+    beta_h * ln g_j := 0 when beta_h == 0 (g^0 = 1); a query whose every key
+    has zero weight outputs zeros;
+  * GQA: query head h reads kv head floor(h / (H_q / H_kv));
+  * RoPE (applied to Q/K at the gathered original positions) is the
+    rotate-half form with inv_freq_i = theta^(-2i/d_h).
+
+Parity status of each function: every function here is pinned by tests that do
+not re-derive it from its own formula (library routines, closed forms, brute
+force, invariants). None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Gate score: Eq. (3) of the deep dive, MLP part; gate value of Eq. (5) read as
+# a sigmoid (see module docstring).
+# ---------------------------------------------------------------------------
+
+def gate_score(h: np.ndarray, W1: np.ndarray, w2: np.ndarray, instr_mask: np.ndarray,
+               b1: Optional[np.ndarray] = None, b2: float = 0.0):
+    """Score every row: u = W1 h (+ b1), a = SiLU(u), s = w2 . a (+ b2), g = sigmoid(s).
+
+    h [T, d], W1 [d_g, d], w2 [d_g], instr_mask [T] (1 = non-prunable).
+    Returns (s [T], g [T]) in float64; g = 1 on non-prunable rows.
+    Deep dive section 3.1, Eq. (3): b~_j = MLP(a~_j); the tokens in the
+    non-prunable set carry no bias (read here as g_j = 1).
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    u = h @ W1.T                                   # [T, d_g]
+    if b1 is not None:
+        u = u + np.asarray(b1, dtype=np.float64)[None, :]
+    with np.errstate(over="ignore"):
+        a = u / (1.0 + np.exp(-u))                 # SiLU(u) = u * sigmoid(u)
+    s = a @ w2 + float(b2)                         # [T]
+    with np.errstate(over="ignore"):
+        g = 1.0 / (1.0 + np.exp(-s))
+    g = np.where(np.asarray(instr_mask) != 0, 1.0, g)
+    return s, g
+
+
+# ---------------------------------------------------------------------------
+# Selection: Eq. (4), S = topK_{j in P}(b_j) U N, with the budget clamped to |P|
+# and kept indices in original order (deep dive section 3.4).
+# ---------------------------------------------------------------------------
+
+def _rank_key(x: float):
+    """Sort key for 'larger score first': NaN last, -0.0 equal to +0.0."""
+    if math.isnan(x):
+        return (1, 0.0)
+    return (0, -(x + 0.0))
+
+
+def topk_select(s: np.ndarray, instr_mask: np.ndarray, cu_seqlens: Sequence[int], K: int):
+    """Keep set per sequence: the K_b = min(K, |P_b|) highest-scoring document rows plus
+    every non-prunable row, listed in ascending row order.
+
+    s [T] fp32 scores (compared exactly as stored), instr_mask [T], cu_seqlens [B+1].
+    Returns (kept_idx int32 [M_total] of global rows, cu_kept int32 [B+1]).
+    """
+    if K < 0:
+        raise ValueError("K must be >= 0")
+    s = np.asarray(s, dtype=np.float32)
+    B = len(cu_seqlens) - 1
+    kept_all = []
+    cu_kept = [0]
+    for b in range(B):
+        start, end = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        prunable = [j for j in range(start, end) if instr_mask[j] == 0]
+        keep_always = [j for j in range(start, end) if instr_mask[j] != 0]
+        K_b = min(K, len(prunable))
+        ranked = sorted(prunable, key=lambda j: (_rank_key(float(s[j])), j))
+        selected = ranked[:K_b]
+        keep = sorted(selected + keep_always)
+        kept_all.extend(keep)
+        cu_kept.append(cu_kept[-1] + len(keep))
+    return np.asarray(kept_all, dtype=np.int32), np.asarray(cu_kept, dtype=np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Gather: deep dive section 3.4, hidden_states[:, keep] and position_ids[:, keep]
+# (original ids), plus the kept gate values (Figure 1 (b)).
+# ---------------------------------------------------------------------------
+
+def gather_kept(h: np.ndarray, pos: Optional[np.ndarray], g: np.ndarray, kept_idx: np.ndarray,
+                cu_seqlens: Sequence[int]):
+    """Rows of h, pos and g at kept_idx. pos None means pos = row - start of its sequence."""
+    kept_idx = np.asarray(kept_idx, dtype=np.int64)
+    h_k = np.asarray(h)[kept_idx]
+    if pos is None:
+        seq_of = np.searchsorted(np.asarray(cu_seqlens), kept_idx, side="right") - 1
+        p_k = (kept_idx - np.asarray(cu_seqlens, dtype=np.int64)[seq_of]).astype(np.int32)
+    else:
+        p_k = np.asarray(pos)[kept_idx]
+    g_k = np.asarray(g)[kept_idx]
+    return h_k, p_k, g_k
+
+
+# ---------------------------------------------------------------------------
+# Token-gated attention: Eq. (5) as the log-space bias form of Eq. (8) with a
+# per-head temperature tau_h and gain beta_h (see module docstring).
+# ---------------------------------------------------------------------------
+
+def _log_bias(g: Optional[np.ndarray], beta: float, n: int) -> np.ndarray:
+    if g is None or beta == 0.0:
+        return np.zeros(n, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        return beta * np.log(np.asarray(g, dtype=np.float64))
+
+
+def gated_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, g: Optional[np.ndarray],
+                    cu_kept: Sequence[int], tau: Sequence[float], beta: Sequence[float],
+                    rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """o_i = sum_{j<=i, same sequence} softmax_j(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j) v_j.
+
+    Q [M, H_q, d_h], K/V [M, H_kv, d_h], g [M] or None (no bias), cu_kept [B+1],
+    tau/beta [H_q]. ``rows`` restricts the output to those global query rows
+    (each row is an independent softmax); the result is [len(rows), H_q, d_h]
+    (or [M, H_q, d_h] when rows is None). Two passes per row: max, then the
+    normalised sum.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    group = H_q // H_kv
+    cu = np.asarray(cu_kept, dtype=np.int64)
+    if rows is None:
+        rows = np.arange(M)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), H_q, d_h), dtype=np.float64)
+    seq_of = np.searchsorted(cu, rows, side="right") - 1
+    inv_sqrt = 1.0 / math.sqrt(d_h)
+    for h in range(H_q):
+        kv = h // group
+        for b in np.unique(seq_of):
+            start = int(cu[b])
+            sel = np.nonzero(seq_of == b)[0]
+            r = rows[sel]
+            end = int(r.max()) + 1
+            keys = K[start:end, kv, :]
+            vals = V[start:end, kv, :]
+            bias = _log_bias(None if g is None else g[start:end], float(beta[h]), end - start)
+            z = (Q[r, h, :] @ keys.T) * inv_sqrt              # [rows, keys]
+            logits = float(tau[h]) * z + bias[None, :]
+            causal = (np.arange(start, end)[None, :] <= r[:, None])
+            logits = np.where(causal, logits, -np.inf)
+            m = logits.max(axis=1, keepdims=True)
+            m_safe = np.where(np.isfinite(m), m, 0.0)
+            p = np.exp(logits - m_safe)                      # exp(-inf) = 0 outside the mask
+            l = p.sum(axis=1, keepdims=True)
+            o = (p @ vals) / np.where(l > 0, l, 1.0)
+            out[sel, h, :] = np.where(l > 0, o, 0.0)
+    return out
+
+
+def gated_attention_weights_eq5(Q: np.ndarray, K: np.ndarray, g: Optional[np.ndarray],
+                                tau: float, beta: float, i: int, h: int = 0,
+                                kv: int = 0) -> np.ndarray:
+    """Eq. (5) product form for one query row of a single sequence:
+    alpha_ij = exp(tau z_ij) g_j^beta / sum_{j'<=i} exp(tau z_ij') g_j'^beta.
+
+    A self-check of the log-bias form used by ``gated_attention``: ln of the
+    product form is the logit plus beta ln g, so the two must agree.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    d_h = Q.shape[-1]
+    z = (K[: i + 1, kv, :] @ Q[i, h, :]) / math.sqrt(d_h)
+    w = np.exp(tau * z)
+    if g is not None and beta != 0.0:
+        w = w * np.power(np.asarray(g[: i + 1], dtype=np.float64), beta)
+    total = w.sum()
+    return w / total if total > 0 else np.zeros_like(w)
+
+
+# ---------------------------------------------------------------------------
+# RoPE at the gathered original positions (deep dive section 3.4 keeps the
+# original position ids; the rotary form is the rotate-half convention).
+# ---------------------------------------------------------------------------
+
+def apply_rope(X: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate each head vector of X [M, H, d_h] by its row's position pos [M].
+
+    Pairs (x_i, x_{i + d_h/2}) rotate by angle pos * theta^(-2i/d_h).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    M, H, d_h = X.shape
+    half = d_h // 2
+    i = np.arange(half, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / d_h)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]   # [M, half]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x1 = X[..., :half]
+    x2 = X[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# The whole prune path (deep dive section 3.4): score -> select -> gather.
+# ---------------------------------------------------------------------------
+
+def gate_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K, b1=None, b2=0.0):
+    s, g = gate_score(h, W1, w2, instr_mask, b1, b2)
+    kept_idx, cu_kept = topk_select(s.astype(np.float32), instr_mask, cu_seqlens, K)
+    h_k, p_k, g_k = gather_kept(h, pos, g, kept_idx, cu_seqlens)
+    return {"s": s, "g": g, "kept_idx": kept_idx, "cu_kept": cu_kept,
+            "h_kept": h_k, "pos_kept": p_k, "g_kept": g_k}

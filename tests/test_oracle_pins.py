@@ -1,0 +1,411 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties an oracle function to a library routine (torch CPU fp64), a
+closed form worked by hand (tests/golden/), a brute-force count, or an
+invariant the TokenGate pages fix. The planted-mistake tests at the end show
+that a dropped term, a flipped sign or a wrong head index fails a pin.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import tokengate_oracle as O
+from learned_token_pruning_07_b300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+pytestmark = pytest.mark.cpu
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Gate score (Eq. 3 MLP, sigmoid gate)
+# ---------------------------------------------------------------------------
+
+def test_gate_score_closed_form():
+    fx = _golden("gate_score_closed_form.json")
+    s, g = O.gate_score(np.array(fx["h"]), np.array(fx["W1"]), np.array(fx["w2"]),
+                        np.array(fx["instr_mask"]))
+    np.testing.assert_allclose(s, fx["s"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(g, fx["g"], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_gate_score_matches_torch_mlp(with_bias):
+    wl = I.WORKLOADS["tiny"]
+    gi = I.make_gate_inputs(wl)
+    h = I.bf16_bits_to_f64(gi["h"])
+    W1 = I.bf16_bits_to_f64(gi["W1"])
+    w2 = I.bf16_bits_to_f64(gi["w2"])
+    rng = np.random.default_rng(5)
+    b1 = rng.standard_normal(wl.d_g) if with_bias else None
+    b2 = 0.3 if with_bias else 0.0
+    s, g = O.gate_score(h, W1, w2, gi["instr_mask"], b1, b2)
+    th = torch.from_numpy(h)
+    lin1 = F.linear(th, torch.from_numpy(W1), None if b1 is None else torch.from_numpy(b1))
+    ref_s = F.linear(F.silu(lin1), torch.from_numpy(w2)[None, :]).squeeze(1) + b2
+    ref_g = torch.sigmoid(ref_s)
+    ref_g[torch.from_numpy(gi["instr_mask"].astype(bool))] = 1.0
+    np.testing.assert_allclose(s, ref_s.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g, ref_g.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_gate_score_zero_initialised_mlp():
+    # The score MLP starts at zero (deep dive section 3.1): every document token scores 0,
+    # so g = sigmoid(0) = 1/2; instruction tokens carry g = 1.
+    wl = I.WORKLOADS["tiny"]
+    gi = I.make_gate_inputs(wl)
+    h = I.bf16_bits_to_f64(gi["h"])
+    s, g = O.gate_score(h, np.zeros((wl.d_g, wl.d)), I.bf16_bits_to_f64(gi["w2"]), gi["instr_mask"])
+    assert np.all(s == 0.0)
+    assert np.all(g[gi["instr_mask"] == 0] == 0.5)
+    assert np.all(g[gi["instr_mask"] == 1] == 1.0)
+
+
+# ---------------------------------------------------------------------------
+# Selection (Eq. 4, clamped budget, original order)
+# ---------------------------------------------------------------------------
+
+def _better(a, b):
+    """a ranks above b (larger first, NaN below everything, -0 == +0)."""
+    if math.isnan(a):
+        return False
+    if math.isnan(b):
+        return True
+    return a > b
+
+
+def _brute_force_keep(s, mask, cu, K):
+    """Pairwise counting: doc row j is selected iff fewer than K_b doc rows beat it."""
+    keep = []
+    cu_out = [0]
+    for b in range(len(cu) - 1):
+        rows = list(range(cu[b], cu[b + 1]))
+        doc = [j for j in rows if mask[j] == 0]
+        K_b = min(K, len(doc))
+        for j in rows:
+            if mask[j]:
+                keep.append(j)
+                continue
+            beaten_by = 0
+            for jj in doc:
+                sj, sjj = float(s[j]), float(s[jj])
+                tie = (sj == sjj) or (math.isnan(sj) and math.isnan(sjj))
+                if _better(sjj, sj) or (tie and jj < j):
+                    beaten_by += 1
+            if beaten_by < K_b:
+                keep.append(j)
+        cu_out.append(len(keep))
+    return np.array(keep, dtype=np.int32), np.array(cu_out, dtype=np.int32)
+
+
+def test_select_worked_example():
+    fx = _golden("select_worked_example.json")
+    for k, want in fx["expected"].items():
+        kept, cu = O.topk_select(np.array(fx["s"], np.float32), np.array(fx["instr_mask"]),
+                                 fx["cu_seqlens"], int(k))
+        assert kept.tolist() == want
+        assert cu.tolist() == [0, len(want)]
+
+
+def _tiny_select_cases():
+    rng = np.random.default_rng(17)
+    cases = []
+    # ties galore: small integer scores
+    for where in ("last", "first", "scattered"):
+        wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(23, 0, 9, 31), instr_lens=(5, 3, 0, 7),
+                            instr_where=where)
+        mask = I.make_instr_mask(wl)
+        s = rng.integers(-3, 4, size=wl.T_total).astype(np.float32)
+        cases.append((s, mask, I.cu_seqlens_of(wl.seq_lens)))
+    # signed zeros, infinities and NaN
+    s = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1.0, -0.0, np.nan, 0.0, -1.0], np.float32)
+    cases.append((s, np.zeros(10, np.uint8), np.array([0, 10], np.int32)))
+    # continuous scores
+    s = rng.standard_normal(40).astype(np.float32)
+    mask = (rng.random(40) < 0.2).astype(np.uint8)
+    cases.append((s, mask, np.array([0, 13, 40], np.int32)))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(5))
+def test_select_matches_brute_force_for_every_budget(case):
+    s, mask, cu = _tiny_select_cases()[case]
+    max_doc = max(int(np.sum(mask[cu[b]:cu[b + 1]] == 0)) for b in range(len(cu) - 1))
+    for K in range(0, max_doc + 2):
+        kept, cu_k = O.topk_select(s, mask, cu, K)
+        ref, ref_cu = _brute_force_keep(s, mask, cu, K)
+        assert kept.tolist() == ref.tolist(), K
+        assert cu_k.tolist() == ref_cu.tolist(), K
+
+
+def test_select_invariants_on_tiny_workload():
+    wl = I.WORKLOADS["tiny"]
+    s = I.make_scores(wl)
+    mask = I.make_instr_mask(wl)
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    n_doc = int(np.sum(mask == 0))
+    for K in (0, 1, 64, n_doc - 1, n_doc, n_doc + 5):
+        kept, cu_k = O.topk_select(s, mask, cu, K)
+        assert np.all(np.diff(kept) > 0)                             # original order, no repeats
+        assert set(np.nonzero(mask)[0]) <= set(kept.tolist())        # N always survives
+        assert len(kept) == min(K, n_doc) + int(mask.sum())          # |S| = K_b + |N|
+        if K >= n_doc:
+            assert kept.tolist() == list(range(wl.T_total))          # full budget keeps all
+        sel = [j for j in kept if mask[j] == 0]
+        rest = [j for j in range(wl.T_total) if mask[j] == 0 and j not in set(sel)]
+        if sel and rest:
+            assert s[sel].min() >= s[rest].max()
+
+
+def test_select_all_equal_scores_keeps_first_k_documents():
+    wl = I.with_changes(I.WORKLOADS["tiny"], instr_where="first")
+    mask = I.make_instr_mask(wl)
+    s = np.full(wl.T_total, 0.25, np.float32)
+    kept, _ = O.topk_select(s, mask, I.cu_seqlens_of(wl.seq_lens), 10)
+    assert kept.tolist() == list(range(32)) + list(range(32, 42))
+
+
+def test_select_on_quantised_ragged_scores_matches_brute_force():
+    wl = I.with_changes(I.WORKLOADS["ragged_b8"], doc_lens=(60, 41, 75), instr_lens=(7, 3, 12),
+                        score_levels=16)
+    s = I.make_scores(wl)
+    assert len(np.unique(s)) < 0.8 * wl.T_total
+    mask = I.make_instr_mask(wl)
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    for K in (0, 5, 20, 40, 80):
+        kept, cu_k = O.topk_select(s, mask, cu, K)
+        ref, ref_cu = _brute_force_keep(s, mask, cu, K)
+        assert kept.tolist() == ref.tolist()
+        assert cu_k.tolist() == ref_cu.tolist()
+
+
+def test_select_rejects_negative_budget():
+    with pytest.raises(ValueError):
+        O.topk_select(np.zeros(4, np.float32), np.zeros(4, np.uint8), [0, 4], -1)
+
+
+# ---------------------------------------------------------------------------
+# Gather (original position ids)
+# ---------------------------------------------------------------------------
+
+def test_gather_default_positions_are_original_ids():
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(20, 30), instr_lens=(4, 6))
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    pos = I.make_positions(wl)
+    rng = np.random.default_rng(3)
+    kept = np.sort(rng.choice(wl.T_total, size=25, replace=False)).astype(np.int32)
+    h = rng.standard_normal((wl.T_total, 8))
+    g = rng.random(wl.T_total)
+    hk, pk, gk = O.gather_kept(h, None, g, kept, cu)
+    hk2, pk2, gk2 = O.gather_kept(h, pos, g, kept, cu)
+    assert pk.tolist() == pk2.tolist()
+    for m, j in enumerate(kept):
+        assert np.array_equal(hk[m], h[j]) and gk[m] == g[j]
+        assert pk[m] == (j if j < cu[1] else j - cu[1])
+
+
+def test_gather_full_keep_is_identity():
+    h = np.arange(12.0).reshape(6, 2)
+    g = np.linspace(0, 1, 6)
+    hk, pk, gk = O.gather_kept(h, None, g, np.arange(6), [0, 6])
+    assert np.array_equal(hk, h) and np.array_equal(gk, g) and pk.tolist() == list(range(6))
+
+
+# ---------------------------------------------------------------------------
+# Token-gated attention (Eq. 5 / Eq. 8)
+# ---------------------------------------------------------------------------
+
+def _sdpa_reference(Q, K, V, g, cu, tau, beta):
+    """torch CPU fp64 scaled_dot_product_attention with an additive float mask
+    (causal -inf plus beta_h ln g_j), scale tau_h / sqrt(d_h), GQA by repeat_interleave."""
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    out = torch.zeros(M, H_q, d_h, dtype=torch.float64)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        if e == a:
+            continue
+        q = torch.from_numpy(Q[a:e]).permute(1, 0, 2)                       # [H_q, n, d]
+        k = torch.from_numpy(K[a:e]).permute(1, 0, 2).repeat_interleave(H_q // H_kv, dim=0)
+        v = torch.from_numpy(V[a:e]).permute(1, 0, 2).repeat_interleave(H_q // H_kv, dim=0)
+        n = e - a
+        causal = torch.full((n, n), float("-inf"), dtype=torch.float64).triu(1)
+        for h in range(H_q):
+            bias = torch.zeros(n, dtype=torch.float64)
+            if g is not None and beta[h] != 0:
+                bias = float(beta[h]) * torch.log(torch.from_numpy(np.asarray(g[a:e], np.float64)))
+            mask = causal + bias[None, :]
+            o = F.scaled_dot_product_attention(q[h:h + 1], k[h:h + 1], v[h:h + 1], attn_mask=mask,
+                                               scale=float(tau[h]) / math.sqrt(d_h))
+            out[a:e, h] = o[0]
+    return out.numpy()
+
+
+def _rand_attn(seed, lens, H_q=4, H_kv=2, d_h=16):
+    rng = np.random.default_rng(seed)
+    M = sum(lens)
+    Q = rng.standard_normal((M, H_q, d_h))
+    K = rng.standard_normal((M, H_kv, d_h))
+    V = rng.standard_normal((M, H_kv, d_h))
+    g = rng.uniform(0.02, 1.0, M)
+    tau = rng.uniform(0.5, 1.5, H_q)
+    beta = rng.uniform(0.5, 1.5, H_q)
+    return Q, K, V, g, I.cu_seqlens_of(lens), tau, beta
+
+
+@pytest.mark.parametrize("lens", [(17,), (5, 33, 1, 12)])
+def test_attention_matches_torch_sdpa_with_bias_mask(lens):
+    Q, K, V, g, cu, tau, beta = _rand_attn(11, lens)
+    got = O.gated_attention(Q, K, V, g, cu, tau, beta)
+    ref = _sdpa_reference(Q, K, V, g, cu, tau, beta)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_attention_beta_zero_is_standard_causal_attention():
+    Q, K, V, g, cu, tau, _ = _rand_attn(12, (29,))
+    beta = np.zeros_like(tau)
+    got = O.gated_attention(Q, K, V, g, cu, tau, beta)
+    q = torch.from_numpy(Q).permute(1, 0, 2)
+    k = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(2, dim=0)
+    v = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(2, dim=0)
+    for h in range(Q.shape[1]):
+        ref = F.scaled_dot_product_attention(q[h:h + 1], k[h:h + 1], v[h:h + 1], is_causal=True,
+                                             scale=float(tau[h]) / math.sqrt(Q.shape[2]))[0]
+        np.testing.assert_allclose(got[:, h], ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_constant_gate_equals_no_gate():
+    Q, K, V, _, cu, tau, beta = _rand_attn(13, (3, 21))
+    g_const = np.full(Q.shape[0], 0.37)
+    a = O.gated_attention(Q, K, V, g_const, cu, tau, beta)
+    b = O.gated_attention(Q, K, V, None, cu, tau, beta)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_eq5_product_form_and_rows_sum_to_one():
+    n = 16
+    rng = np.random.default_rng(14)
+    Q = rng.standard_normal((n, 1, n))
+    K = rng.standard_normal((n, 1, n))
+    V = np.eye(n)[:, None, :]                      # o_i = the weight vector alpha_i
+    g = rng.uniform(0.05, 1.0, n)
+    tau, beta = np.array([1.3]), np.array([0.7])
+    o = O.gated_attention(Q, K, V, g, [0, n], tau, beta)[:, 0, :]
+    for i in range(n):
+        w = O.gated_attention_weights_eq5(Q, K, g, 1.3, 0.7, i)
+        np.testing.assert_allclose(o[i, :i + 1], w, rtol=1e-12, atol=1e-14)
+        assert np.all(o[i, i + 1:] == 0.0)
+        assert abs(o[i].sum() - 1.0) < 1e-12
+
+
+def test_attention_zero_logits_closed_form():
+    fx = _golden("attention_zero_logits.json")
+    got = O.gated_attention(np.array(fx["Q"]), np.array(fx["K"]), np.array(fx["V"]),
+                            np.array(fx["g"]), [0, 3], fx["tau"], fx["beta"])
+    np.testing.assert_allclose(got, np.array(fx["O"]), rtol=0, atol=1e-15)
+
+
+def test_attention_single_token_returns_its_value():
+    Q, K, V, g, _, tau, beta = _rand_attn(15, (1,))
+    got = O.gated_attention(Q, K, V, g, [0, 1], tau, beta)
+    np.testing.assert_allclose(got[0], np.repeat(V[0], 2, axis=0), rtol=0, atol=0)
+
+
+def test_attention_tiny_gate_removes_key():
+    Q, K, V, g, cu, tau, _ = _rand_attn(16, (12,))
+    beta = np.ones_like(tau)
+    g = g.copy()
+    g[4] = 1e-300
+    got = O.gated_attention(Q, K, V, g, cu, tau, beta)
+    keep = [j for j in range(12) if j != 4]
+    sub = O.gated_attention(Q[keep], K[keep], V[keep], g[keep], [0, 11], tau, beta)
+    np.testing.assert_allclose(got[keep], sub, rtol=1e-9, atol=1e-12)
+
+
+def test_attention_all_zero_gates_give_zero_rows():
+    Q, K, V, _, cu, tau, beta = _rand_attn(17, (6,))
+    g = np.zeros(6)
+    got = O.gated_attention(Q, K, V, g, cu, tau, beta)
+    assert np.all(got == 0.0)
+
+
+def test_attention_sequences_are_independent_and_rows_subset():
+    Q, K, V, g, cu, tau, beta = _rand_attn(18, (9, 14))
+    whole = O.gated_attention(Q, K, V, g, cu, tau, beta)
+    second = O.gated_attention(Q[9:], K[9:], V[9:], g[9:], [0, 14], tau, beta)
+    np.testing.assert_allclose(whole[9:], second, rtol=1e-12, atol=1e-14)
+    rows = [0, 8, 9, 22]
+    np.testing.assert_allclose(O.gated_attention(Q, K, V, g, cu, tau, beta, rows=rows), whole[rows],
+                               rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def test_rope_matches_complex_rotation_and_is_relative():
+    rng = np.random.default_rng(19)
+    M, H, d_h = 7, 3, 8
+    X = rng.standard_normal((M, H, d_h))
+    pos = rng.integers(0, 5000, M)
+    out = O.apply_rope(X, pos, 1.0e6)
+    half = d_h // 2
+    z = X[..., :half] + 1j * X[..., half:]
+    freq = 1.0e6 ** (-np.arange(half) * 2.0 / d_h)
+    zr = z * np.exp(1j * pos[:, None, None] * freq[None, None, :])
+    np.testing.assert_allclose(out, np.concatenate([zr.real, zr.imag], axis=-1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(O.apply_rope(X, np.zeros(M, int), 1e6), X)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=-1), np.linalg.norm(X, axis=-1), rtol=1e-12)
+    q, k = X[:1], X[1:2]
+    a = O.apply_rope(q, np.array([40]), 1e4)[0, 0] @ O.apply_rope(k, np.array([25]), 1e4)[0, 0]
+    b = O.apply_rope(q, np.array([1040]), 1e4)[0, 0] @ O.apply_rope(k, np.array([1025]), 1e4)[0, 0]
+    assert abs(a - b) < 1e-9
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each variant must fail at least one pin above
+# ---------------------------------------------------------------------------
+
+def _planted_attention(kind):
+    def f(Q, K, V, g, cu_kept, tau, beta, rows=None):
+        if kind == "bias_sign":
+            return O.gated_attention(Q, K, V, None if g is None else 1.0 / np.asarray(g), cu_kept, tau, beta, rows)
+        if kind == "no_tau":
+            return O.gated_attention(Q, K, V, g, cu_kept, np.ones_like(tau), beta, rows)
+        if kind == "gqa_modulo":
+            H_q, H_kv = Q.shape[1], K.shape[1]
+            Kp = np.stack([K[:, h % H_kv] for h in range(H_q)], axis=1)
+            Vp = np.stack([V[:, h % H_kv] for h in range(H_q)], axis=1)
+            return O.gated_attention(Q, Kp, Vp, g, cu_kept, tau, beta, rows)
+        raise ValueError(kind)
+    return f
+
+
+@pytest.mark.parametrize("kind", ["bias_sign", "no_tau", "gqa_modulo"])
+def test_planted_attention_mistakes_fail_the_sdpa_pin(kind):
+    Q, K, V, g, cu, tau, beta = _rand_attn(11, (17,))
+    got = _planted_attention(kind)(Q, K, V, g, cu, tau, beta)
+    ref = _sdpa_reference(Q, K, V, g, cu, tau, beta)
+    assert not np.allclose(got, ref, rtol=1e-6, atol=1e-8)
+
+
+def test_planted_selection_mistake_fails_brute_force():
+    # ties to the higher index instead of the lower one
+    s, mask, cu = _tiny_select_cases()[0]
+    kept_bad = []
+    for b in range(len(cu) - 1):
+        rows = range(cu[b], cu[b + 1])
+        doc = [j for j in rows if mask[j] == 0]
+        ranked = sorted(doc, key=lambda j: (-float(s[j]), -j))[:min(5, len(doc))]
+        kept_bad.extend(sorted(ranked + [j for j in rows if mask[j]]))
+    ref, _ = _brute_force_keep(s, mask, cu, 5)
+    assert kept_bad != ref.tolist()
