@@ -1,0 +1,202 @@
+/*
+ * tokengate.h — C ABI of libtokengate, the B300 (sm_103a) TokenGate gated-prefill path.
+ *
+ * The path (TokenGate paper deep dive, agientry.com, sections 3.1-3.4; TokenGate paper
+ * page, thelatestinai.com, Figure 1): at the gate layer a small MLP scores every hidden
+ * state, a top-K selector keeps the K highest-scoring document tokens plus every
+ * non-prunable (instruction / question) token in original order, the kept rows, their
+ * original position ids and gate values are gathered, and the layers above run
+ * token-gated causal GQA attention over the kept tokens only.
+ *
+ * Conventions shared by every entry point
+ *  - Every function returns a tg_status. TG_OK means the work was enqueued (or done).
+ *  - Pointers marked [device] are device memory owned by the caller; the library never
+ *    allocates, frees or retains them beyond the call. Pointers marked [host] are read
+ *    during the call only.
+ *  - bf16 tensors are passed as uint16_t* holding bf16 bit patterns.
+ *  - All work is enqueued asynchronously on the caller's stream (NULL = legacy default).
+ *  - Host scalars are validated before anything is launched; a bad one returns
+ *    TG_ERR_INVALID_ARG (or TG_ERR_UNSUPPORTED for a legal shape the kernels do not
+ *    tile) and launches nothing.
+ *  - Conditions only the device can see (cu_seqlens that are not a non-decreasing
+ *    partition of [0, T_total], an index out of range, an output that would pass its
+ *    capacity, a pipeline wait that gave up) are reported through the caller's int32
+ *    `status` word in device memory: the kernels OR in a TG_DEV_* bit and never touch
+ *    memory out of bounds. The caller zeroes the word; tg_read_device_status() fetches it.
+ *  - Launch errors are returned as TG_ERR_CUDA; tg_last_cuda_error() gives the code.
+ *  - No NaN policy is imposed on data; top-K ranks NaN below every number.
+ */
+#ifndef TOKENGATE_H_
+#define TOKENGATE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TG_API __attribute__((visibility("default")))
+#else
+#define TG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tg_stream_t; /* the same handle as cudaStream_t */
+
+typedef int32_t tg_status;
+enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1,
+  TG_ERR_UNSUPPORTED = 2,
+  TG_ERR_CUDA = 3,
+  TG_ERR_CAPACITY = 4,
+  TG_ERR_DEVICE_TIMEOUT = 5,
+  TG_ERR_DEVICE = 6
+};
+
+/* Bits the kernels OR into the caller's device status word. */
+enum {
+  TG_DEV_BAD_SEQLENS = 1 << 0, /* cu_seqlens / cu_kept not a valid partition          */
+  TG_DEV_BAD_INDEX = 1 << 1,   /* a kept index outside [0, T_total)                      */
+  TG_DEV_CAPACITY = 1 << 2,    /* output would pass its capacity; the excess was dropped */
+  TG_DEV_TIMEOUT = 1 << 3      /* a pipeline wait gave up; outputs are not valid          */
+};
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+TG_API int32_t tg_version(void);
+
+/* Human-readable name of a status code (static storage). */
+TG_API const char *tg_status_string(tg_status s);
+
+/* The last CUDA runtime error seen by any entry point on this thread (cudaError_t value). */
+TG_API int32_t tg_last_cuda_error(void);
+
+/*
+ * tg_gate_score — score every row (deep dive section 3.1, Eq. (3): b~_j = MLP(a~_j)).
+ *   u = W1 h_j (+ b1), s_j = w2 . SiLU(u) (+ b2), g_j = sigmoid(s_j); g_j = 1 on
+ *   non-prunable rows (they carry zero log-bias, the reading of "b_j := 0 for j in N").
+ *   h          [device] bf16 [T_total, d], row-major (token-major), 16-byte aligned.
+ *   instr_mask [device] uint8 [T_total], 1 = non-prunable. May be NULL (no such rows).
+ *   W1         [device] bf16 [d_g, d], row-major, 16-byte aligned.
+ *   b1         [device] fp32 [d_g] or NULL.   w2 [device] bf16 [d_g].   b2: host scalar.
+ *   s_out      [device] fp32 [T_total]: the fp32 score that top-K ranks.
+ *   g_out      [device] fp32 [T_total]: the gate value. May be NULL.
+ *   status     [device] int32 word (TG_DEV_TIMEOUT).
+ *   Shapes: d % 32 == 0, d_g % 32 == 0, 32 <= d_g <= 512; else TG_ERR_UNSUPPORTED.
+ *   Compute: bf16 tcgen05 MMA with fp32 accumulation in tensor memory; fp32 epilogue.
+ */
+TG_API tg_status tg_gate_score(const uint16_t *h, int32_t T_total, int32_t d, const uint8_t *instr_mask,
+                        const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                        int32_t d_g, float *s_out, float *g_out, int32_t *status,
+                        tg_stream_t stream);
+
+/*
+ * tg_topk_select — the retained set (deep dive section 3.1, Eq. (4): S = topK_{j in P}(b_j)
+ *   union N; section 3.4: the budget is clamped to |P| and the keep indices are built over
+ *   the full sequence in original order).
+ *   For each sequence b: K_b = min(K, |P_b|) document rows with the largest s (ties to the
+ *   lower row; -0.0 ranks as +0.0; NaN below every number), plus every row with
+ *   instr_mask = 1, written in ascending row order.
+ *   s          [device] fp32 [T_total].     instr_mask [device] uint8 [T_total] or NULL.
+ *   cu_seqlens [device] int32 [B+1], a non-decreasing partition of [0, T_total].
+ *   kept_idx   [device] int32 [capacity]: global row of each kept token.
+ *   cu_kept    [device] int32 [B+1]: cu_kept[b+1] - cu_kept[b] = K_b + |N_b|.
+ *   A capacity of T_total is always enough. Rows past capacity are dropped and
+ *   TG_DEV_CAPACITY is set; cu_kept still reports the untruncated counts.
+ *   Limits: 1 <= B <= 1024 (else TG_ERR_UNSUPPORTED), K >= 0.
+ */
+TG_API tg_status tg_topk_select(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
+                         int32_t B, int32_t T_total, int32_t K, int32_t *kept_idx,
+                         int32_t capacity, int32_t *cu_kept, int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_gather_kept — slice the hidden states and gather the original position ids and gate
+ *   values of the kept rows (deep dive section 3.4: hidden_states[:, keep] and
+ *   position_ids[:, keep]; paper page Figure 1 (b): kept states travel with their scores).
+ *   h        [device] bf16 [T_total, d], 16-byte aligned rows (d % 8 == 0).
+ *   pos      [device] int32 [T_total] or NULL (then pos = row - cu_seqlens[b]).
+ *   g        [device] fp32 [T_total] or NULL (then g_kept is not written).
+ *   kept_idx, cu_kept as written by tg_topk_select; rows m < min(cu_kept[B], capacity).
+ *   h_kept   [device] bf16 [capacity, d].  pos_kept [device] int32 [capacity] or NULL.
+ *   g_kept   [device] fp32 [capacity] or NULL.
+ *   status   [device] int32 word (TG_DEV_BAD_INDEX) or NULL.
+ */
+TG_API tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g,
+                         const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
+                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
+                         tg_stream_t stream);
+
+/*
+ * tg_gated_attention — token-gated causal GQA attention over the kept tokens
+ *   (deep dive section 3.2, Eq. (5) and Eq. (8), in log-bias form):
+ *     o_i = sum_{j <= i, same sequence} softmax_j(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j) v_j
+ *   With beta_h = 1 each attention weight is multiplied by its key's gate value and
+ *   renormalised (paper page Figure 1 (c)). beta_h ln g_j is taken as 0 when beta_h = 0.
+ *   Query head h reads kv head h / (H_q / H_kv). A query whose every key has zero weight
+ *   outputs zeros.
+ *   Q [device] bf16 [M, H_q, d_h];  K, V [device] bf16 [M, H_kv, d_h]; token-major, dense.
+ *   g [device] fp32 [M] or NULL (no bias).
+ *   cu_kept [device] int32 [B+1]: sequence boundaries in the kept rows; rows are clamped
+ *     to M_capacity.
+ *   max_seqlen: host upper bound on any cu_kept[b+1] - cu_kept[b] (sizes the grid;
+ *     longer sequences set TG_DEV_BAD_SEQLENS).
+ *   tau, beta [host] fp32 [H_q]; tau > 0 finite, beta >= 0 finite.
+ *   O [device] bf16 [M, H_q, d_h].   status [device] int32 word.
+ *   Shapes: d_h == 128 or 64, H_q % H_kv == 0, H_q <= 128; else TG_ERR_UNSUPPORTED.
+ *   Compute: bf16 tcgen05 MMA, fp32 softmax and accumulation.
+ */
+TG_API tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                             const float *g, const int32_t *cu_kept, int32_t B,
+                             int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                             int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                             int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_gate_prune_layer — tg_gate_score, tg_topk_select and tg_gather_kept enqueued back to
+ *   back on one stream (the deep dive's section 3.4 prune path: score, clamp, select, keep
+ *   indices, slice hidden states, gather positions). Arguments as in the three calls;
+ *   s_out and g_out are required here (they are the intermediate buffers).
+ */
+TG_API tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                              const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                              const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                              int32_t d_g, int32_t K, float *s_out, float *g_out,
+                              int32_t *kept_idx, int32_t capacity, int32_t *cu_kept,
+                              uint16_t *h_kept, int32_t *pos_kept, float *g_kept,
+                              int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_apply_rope — rotate Q or K rows in place at their original position ids (rotate-half
+ *   form, inv_freq_i = theta^(-2i/d_h)); the deep dive (section 3.4) keeps the original
+ *   position ids for the kept tokens.
+ *   X [device] bf16 [capacity, H, d_h];  pos [device] int32 [capacity].
+ *   cu_kept [device] int32 [B+1] or NULL: when given, only rows < min(cu_kept[B], capacity)
+ *   are touched; when NULL, all `capacity` rows are.
+ *   d_h even, d_h <= 256; theta > 0.
+ */
+TG_API tg_status tg_apply_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
+                        int32_t capacity, int32_t H, int32_t d_h, float theta,
+                        tg_stream_t stream);
+
+/*
+ * tg_read_device_status — synchronise `stream`, copy the device status word to *out and
+ *   translate it: 0 -> TG_OK, TG_DEV_TIMEOUT -> TG_ERR_DEVICE_TIMEOUT, TG_DEV_CAPACITY ->
+ *   TG_ERR_CAPACITY, any other bit -> TG_ERR_DEVICE. *out receives the raw bits.
+ */
+TG_API tg_status tg_read_device_status(const int32_t *status, int32_t *out, tg_stream_t stream);
+
+/*
+ * tg_set_wait_limit_ns — upper bound, in nanoseconds of device time, on any single
+ *   pipeline wait inside the tensor-core kernels (default 2e9, i.e. two seconds). A wait
+ *   that runs past it sets TG_DEV_TIMEOUT, drains the copies it started and returns.
+ *   0 restores the default. Process-wide; takes effect for later launches.
+ */
+TG_API tg_status tg_set_wait_limit_ns(uint64_t limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOKENGATE_H_ */

@@ -1,0 +1,171 @@
+"""ctypes binding of libtokengate (include/tokengate.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module turns torch
+tensors into raw pointers and sizes, calls the C entry point of the same name and
+raises on a non-OK status. There is no fallback: if the library is missing or a call
+fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtokengate.so")
+
+TG_OK, TG_ERR_INVALID_ARG, TG_ERR_UNSUPPORTED, TG_ERR_CUDA = 0, 1, 2, 3
+TG_ERR_CAPACITY, TG_ERR_DEVICE_TIMEOUT, TG_ERR_DEVICE = 4, 5, 6
+TG_DEV_BAD_SEQLENS, TG_DEV_BAD_INDEX, TG_DEV_CAPACITY, TG_DEV_TIMEOUT = 1, 2, 4, 8
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_F = ctypes.c_float
+
+# name -> (restype, argtypes); mirrors include/tokengate.h
+SIGNATURES = {
+    "tg_version": (_I, []),
+    "tg_status_string": (ctypes.c_char_p, [_I]),
+    "tg_last_cuda_error": (_I, []),
+    "tg_gate_score": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P]),
+    "tg_topk_select": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "tg_gather_kept": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "tg_gated_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_gate_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
+                                 _P, _P, _P, _P, _P, _P]),
+    "tg_apply_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "tg_read_device_status": (_I, [_P, _P, _P]),
+    "tg_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+}
+
+
+class TGError(RuntimeError):
+    def __init__(self, name: str, status: int, msg: str):
+        super().__init__(f"{name} failed: status {status} ({msg})")
+        self.status = status
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtokengate.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m learned_token_pruning_07_b300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check(name: str, status: int):
+    if status != TG_OK:
+        lib = load()
+        msg = lib.tg_status_string(status).decode()
+        if status == TG_ERR_CUDA:
+            msg += f", cudaError {lib.tg_last_cuda_error()}"
+        raise TGError(name, status, msg)
+
+
+def _host_f32(x):
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    return a, a.ctypes.data
+
+
+# ---------------------------------------------------------------------------
+# Entry points (tensors are torch CUDA tensors; bf16 data as torch.bfloat16 or int16/uint16)
+# ---------------------------------------------------------------------------
+
+def gate_score(h, W1, w2, s_out, g_out=None, instr_mask=None, b1=None, b2: float = 0.0,
+               status=None, stream=None):
+    T, d = h.shape
+    d_g = W1.shape[0]
+    st = load().tg_gate_score(_ptr(h), T, d, _ptr(instr_mask), _ptr(W1), _ptr(b1), _ptr(w2), float(b2),
+                              d_g, _ptr(s_out), _ptr(g_out), _ptr(status), _stream(stream))
+    _check("tg_gate_score", st)
+
+
+def topk_select(s, cu_seqlens, K: int, kept_idx, cu_kept, instr_mask=None, status=None, stream=None):
+    B = cu_seqlens.numel() - 1
+    st = load().tg_topk_select(_ptr(s), _ptr(instr_mask), _ptr(cu_seqlens), B, s.numel(), int(K),
+                               _ptr(kept_idx), kept_idx.numel(), _ptr(cu_kept), _ptr(status),
+                               _stream(stream))
+    _check("tg_topk_select", st)
+
+
+def gather_kept(h, cu_seqlens, kept_idx, cu_kept, h_kept, pos=None, g=None, pos_kept=None,
+                g_kept=None, status=None, stream=None):
+    T, d = h.shape
+    B = cu_seqlens.numel() - 1
+    st = load().tg_gather_kept(_ptr(h), _ptr(pos), _ptr(g), _ptr(cu_seqlens), B, T, d, _ptr(kept_idx),
+                               _ptr(cu_kept), h_kept.shape[0], _ptr(h_kept), _ptr(pos_kept),
+                               _ptr(g_kept), _ptr(status), _stream(stream))
+    _check("tg_gather_kept", st)
+
+
+def gated_attention(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, status=None,
+                    stream=None):
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    B = cu_kept.numel() - 1
+    tau_a, tau_p = _host_f32(tau)
+    beta_a, beta_p = _host_f32(beta)
+    st = load().tg_gated_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(cu_kept), B, M,
+                                   int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O),
+                                   _ptr(status), _stream(stream))
+    del tau_a, beta_a
+    _check("tg_gated_attention", st)
+
+
+def gate_prune_layer(h, cu_seqlens, W1, w2, K: int, s_out, g_out, kept_idx, cu_kept, h_kept,
+                     pos_kept=None, g_kept=None, pos=None, instr_mask=None, b1=None, b2: float = 0.0,
+                     status=None, stream=None):
+    T, d = h.shape
+    B = cu_seqlens.numel() - 1
+    st = load().tg_gate_prune_layer(_ptr(h), _ptr(pos), _ptr(instr_mask), _ptr(cu_seqlens), B, T, d,
+                                    _ptr(W1), _ptr(b1), _ptr(w2), float(b2), W1.shape[0], int(K),
+                                    _ptr(s_out), _ptr(g_out), _ptr(kept_idx), kept_idx.numel(),
+                                    _ptr(cu_kept), _ptr(h_kept), _ptr(pos_kept), _ptr(g_kept),
+                                    _ptr(status), _stream(stream))
+    _check("tg_gate_prune_layer", st)
+
+
+def apply_rope(X, pos, theta: float, cu_kept=None, stream=None):
+    cap, H, d_h = X.shape
+    B = 0 if cu_kept is None else cu_kept.numel() - 1
+    st = load().tg_apply_rope(_ptr(X), _ptr(pos), _ptr(cu_kept), B, cap, H, d_h, float(theta),
+                              _stream(stream))
+    _check("tg_apply_rope", st)
+
+
+def read_device_status(status, stream=None) -> int:
+    """Synchronise and return the raw device status bits (0 = ok)."""
+    out = ctypes.c_int32(0)
+    st = load().tg_read_device_status(_ptr(status), ctypes.addressof(out), _stream(stream))
+    if st in (TG_ERR_INVALID_ARG, TG_ERR_CUDA):
+        _check("tg_read_device_status", st)
+    return out.value
+
+
+def set_wait_limit_ns(ns: int):
+    _check("tg_set_wait_limit_ns", load().tg_set_wait_limit_ns(int(ns)))

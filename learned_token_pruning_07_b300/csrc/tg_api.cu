@@ -1,0 +1,149 @@
+// tg_api.cu — the extern "C" entry points of libtokengate: argument validation on the host,
+// then the launches in tg_score.cu / tg_select.cu / tg_gather.cu / tg_attention.cu.
+#include <cmath>
+
+#include "tg_common.cuh"
+
+namespace tg_host {
+tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8_t *mask,
+                            const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                            int32_t d_g, float *s_out, float *g_out, int32_t *status,
+                            cudaStream_t stream);
+tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
+                             int32_t B, int32_t T, int32_t K, int32_t *kept_idx, int32_t capacity,
+                             int32_t *cu_kept, int32_t *status, cudaStream_t stream);
+tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
+                        const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t d,
+                        const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
+                        uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
+                        cudaStream_t stream);
+tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
+                      int32_t capacity, int32_t H, int32_t d_h, float theta, cudaStream_t stream);
+tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                 int32_t *status, cudaStream_t stream);
+}  // namespace tg_host
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t S(tg_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+constexpr int32_t kMaxSelectB = 1024;
+
+tg_status check_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint16_t *W1,
+                           const uint16_t *w2, int32_t d_g, const float *s_out, float b2) {
+  if (!h || !W1 || !w2 || !s_out) return TG_ERR_INVALID_ARG;
+  if (T < 0 || d <= 0 || d_g <= 0 || !std::isfinite(b2)) return TG_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W1)) return TG_ERR_INVALID_ARG;
+  if (d % 32 != 0 || d_g % 32 != 0 || d_g > 512) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+tg_status check_select(const float *s, const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t K,
+                       const int32_t *kept_idx, int32_t capacity, const int32_t *cu_kept) {
+  if (!s || !cu_seqlens || !cu_kept) return TG_ERR_INVALID_ARG;
+  if (B < 1 || T < 0 || K < 0 || capacity < 0) return TG_ERR_INVALID_ARG;
+  if (capacity > 0 && !kept_idx) return TG_ERR_INVALID_ARG;
+  if (B > kMaxSelectB) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+tg_status check_gather(const uint16_t *h, const int32_t *cu_seqlens, int32_t B, int32_t T,
+                       int32_t d, const int32_t *kept_idx, const int32_t *cu_kept,
+                       int32_t capacity, const uint16_t *h_kept) {
+  if (!h || !cu_seqlens || !kept_idx || !cu_kept || !h_kept) return TG_ERR_INVALID_ARG;
+  if (B < 1 || T < 0 || d <= 0 || capacity < 0) return TG_ERR_INVALID_ARG;
+  if (d % 8 != 0 || !aligned16(h) || !aligned16(h_kept)) return TG_ERR_INVALID_ARG;
+  return TG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tg_status tg_gate_score(const uint16_t *h, int32_t T_total, int32_t d, const uint8_t *instr_mask,
+                        const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                        int32_t d_g, float *s_out, float *g_out, int32_t *status,
+                        tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1, w2, d_g, s_out, b2);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, w2, b2, d_g, s_out, g_out,
+                                    status, S(stream));
+}
+
+tg_status tg_topk_select(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
+                         int32_t B, int32_t T_total, int32_t K, int32_t *kept_idx,
+                         int32_t capacity, int32_t *cu_kept, int32_t *status, tg_stream_t stream) {
+  tg_status st = check_select(s, cu_seqlens, B, T_total, K, kept_idx, capacity, cu_kept);
+  if (st != TG_OK) return st;
+  return tg_host::launch_topk_select(s, instr_mask, cu_seqlens, B, T_total, K, kept_idx, capacity,
+                                     cu_kept, status, S(stream));
+}
+
+tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g,
+                         const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
+                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
+                         tg_stream_t stream) {
+  tg_status st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity, h_kept);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gather(h, pos, g, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity,
+                                h_kept, pos_kept, g_kept, status, S(stream));
+}
+
+tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                             const float *g, const int32_t *cu_kept, int32_t B,
+                             int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                             int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                             int32_t *status, tg_stream_t stream) {
+  if (!Q || !K || !V || !cu_kept || !tau || !beta || !O) return TG_ERR_INVALID_ARG;
+  if (B < 1 || M_capacity < 0 || max_seqlen < 0 || H_q < 1 || H_kv < 1 || d_h < 1)
+    return TG_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TG_ERR_INVALID_ARG;
+  for (int h = 0; h < H_q && h < 128; ++h) {
+    if (!std::isfinite(tau[h]) || !(tau[h] > 0.0f)) return TG_ERR_INVALID_ARG;
+    if (!std::isfinite(beta[h]) || beta[h] < 0.0f) return TG_ERR_INVALID_ARG;
+  }
+  if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
+  return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
+                                         d_h, tau, beta, O, status, S(stream));
+}
+
+tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                              const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                              const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                              int32_t d_g, int32_t K, float *s_out, float *g_out,
+                              int32_t *kept_idx, int32_t capacity, int32_t *cu_kept,
+                              uint16_t *h_kept, int32_t *pos_kept, float *g_kept,
+                              int32_t *status, tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1, w2, d_g, s_out, b2);
+  if (st == TG_OK && !g_out) st = TG_ERR_INVALID_ARG;
+  if (st == TG_OK) st = check_select(s_out, cu_seqlens, B, T_total, K, kept_idx, capacity, cu_kept);
+  if (st == TG_OK)
+    st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity, h_kept);
+  if (st != TG_OK) return st;
+  st = tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, w2, b2, d_g, s_out, g_out,
+                                  status, S(stream));
+  if (st != TG_OK) return st;
+  st = tg_host::launch_topk_select(s_out, instr_mask, cu_seqlens, B, T_total, K, kept_idx,
+                                   capacity, cu_kept, status, S(stream));
+  if (st != TG_OK) return st;
+  return tg_host::launch_gather(h, pos, g_out, cu_seqlens, B, T_total, d, kept_idx, cu_kept,
+                                capacity, h_kept, pos_kept, g_kept, status, S(stream));
+}
+
+tg_status tg_apply_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
+                        int32_t capacity, int32_t H, int32_t d_h, float theta,
+                        tg_stream_t stream) {
+  if (!X || !pos) return TG_ERR_INVALID_ARG;
+  if (capacity < 0 || H < 1 || d_h < 2 || d_h % 2 != 0 || !(theta > 0.0f) || !std::isfinite(theta))
+    return TG_ERR_INVALID_ARG;
+  if (cu_kept && B < 1) return TG_ERR_INVALID_ARG;
+  if (d_h > 256) return TG_ERR_UNSUPPORTED;
+  return tg_host::launch_rope(X, pos, cu_kept, B, capacity, H, d_h, theta, S(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,496 @@
+// tg_attention.cu — token-gated causal GQA attention over the kept tokens (TokenGate deep
+// dive, section 3.2: Eq. (5), alpha_ij proportional to exp(z_ij) g_j; Eq. (8) with the gate
+// as a per-key, per-head bias inside the softmax and a temperature on the logits).
+//
+//   o_i = sum_{j<=i} softmax_j( tau_h * q_i.k_j / sqrt(d_h) + beta_h * ln g_j ) v_j
+//
+// Computed in base 2: x_ij = s_ij * (tau_h log2(e) / sqrt(d_h)) + beta_h log2(g_j), p = 2^(x - m).
+//
+// One CTA handles one 128-row query tile of one sequence for TWO query heads that read the
+// same kv head (a GQA pair), so every K/V tile brought in by TMA feeds two Q tiles. Tensor
+// memory (512 columns) holds S_0, S_1 (fp32 128x128 each; P_t is written back over S_t as
+// packed bf16) and the output accumulators O_0, O_1 (fp32 128 x d_h).
+// Warp roles (12 warps):
+//   warp 0       TMA producer: Q tiles once, then the K/V ring (kStages deep)
+//   warp 1       tensor-memory owner and MMA issuer:  S_t = Q_t K^T ; O_t += P_t V
+//   warps 4-7    softmax + correction + epilogue for Q tile 0 (thread = query row = TMEM lane)
+//   warps 8-11   the same for Q tile 1
+// Online softmax with a lazily updated running max: the reference max m only moves when the
+// tile max exceeds it by more than 8 (log2 units), so the O rescale (a TMEM read-modify-write)
+// is rare; the result is exact either way because O and l share the same reference.
+#include "tg_common.cuh"
+
+namespace {
+
+constexpr int kBlockM = 128;      // query rows per tile
+constexpr int kBlockN = 128;      // keys per KV tile
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxHeads = 128;
+
+template <int D>
+struct AttnCfg {
+  static constexpr int kHalves = D / 64;                    // 128-byte swizzle atoms per row
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;     // one 128-row bf16 tile
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = 2 * kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+  static constexpr uint32_t kOffBias = kOffV + kStages * kTileBytes;       // [2 tiles][2][128] f32
+  static constexpr uint32_t kOffBar = kOffBias + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+};
+
+struct AttnParams {
+  const float *g;
+  const int32_t *cu_kept;
+  int32_t B, M_cap, max_seqlen, H_q, H_kv, group, heads_per_cta, pairs, n_qt_max;
+  uint16_t *O;
+  int32_t *status;
+  uint64_t wait_limit;
+  float scale_log2[kMaxHeads];  // tau_h * log2(e) / sqrt(d_h)
+  float beta[kMaxHeads];
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Barrier over the `n` threads of named barrier `id` that also ANDs a predicate across them,
+// so a give-up decision is taken by the whole warpgroup at once.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    gated_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ AttnParams p) {
+  using C = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = smem + C::kOffQ;
+  uint8_t *sK = smem + C::kOffK;
+  uint8_t *sV = smem + C::kOffV;
+  float *sBias = reinterpret_cast<float *>(smem + C::kOffBias);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *q_full = bars;
+  uint64_t *kv_full = bars + 1;
+  uint64_t *kv_empty = kv_full + C::kStages;
+  uint64_t *s_full = kv_empty + C::kStages;  // [2]
+  uint64_t *p_full = s_full + 2;             // [2]
+  uint64_t *o_final = p_full + 2;            // [2]
+  uint64_t *pv_done = o_final + 2;           // [2]
+  uint64_t *drain = pv_done + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
+  int32_t *n_issued = abort_flag + 1;
+  int32_t *n_consumed = abort_flag + 2;
+  volatile int32_t *vabort = abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: heaviest (last) query tiles first ----
+  const int item = blockIdx.x;
+  const int hp = item % p.pairs;
+  const int rest = item / p.pairs;
+  const int b = rest % p.B;
+  const int tq = p.n_qt_max - 1 - rest / p.B;
+  int seq_start = p.cu_kept[b];
+  int seq_end = p.cu_kept[b + 1];
+  if (seq_start < 0 || seq_end < seq_start || seq_end - seq_start > p.max_seqlen) {
+    if (threadIdx.x == 0 && tq == p.n_qt_max - 1 && hp == 0) tg::report(p.status, TG_DEV_BAD_SEQLENS);
+    return;
+  }
+  seq_start = min(seq_start, p.M_cap);
+  seq_end = min(seq_end, p.M_cap);
+  const int seq_len = seq_end - seq_start;
+  const int q0 = tq * kBlockM;
+  if (q0 >= seq_len) return;  // uniform for the CTA
+  const int n_kv = tq + 1;    // causal: key tiles 0..tq
+  const int h0 = hp * p.heads_per_cta;
+  const int kvh = h0 / p.group;
+  const int n_tiles = p.heads_per_cta;  // Q tiles in this CTA (1 or 2)
+
+  if (threadIdx.x == 0) {
+    tg::mbar_init(q_full, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      tg::mbar_init(&kv_full[i], 1);
+      tg::mbar_init(&kv_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      tg::mbar_init(&s_full[t], 1);
+      tg::mbar_init(&p_full[t], 128);
+      tg::mbar_init(&o_final[t], 1);
+      tg::mbar_init(&pv_done[t], 1);
+    }
+    tg::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *n_issued = 0;
+    *n_consumed = 0;
+    tg::fence_mbar_init();
+    tg::prefetch_tensormap(&tm_q);
+    tg::prefetch_tensormap(&tm_k);
+    tg::prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tg::tmem_alloc(tmem_slot, 512);
+    tg::tmem_relinquish();
+  }
+  tg::tc_fence_before();
+  __syncthreads();
+  tg::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tg::mbar_arrive_expect_tx(q_full, n_tiles * C::kTileBytes);
+      for (int t = 0; t < n_tiles; ++t)
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tg::tma_load_3d(sQ + t * C::kTileBytes + hf * 16384, &tm_q, q_full, hf * 64, h0 + t,
+                          seq_start + q0);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!tg::mbar_wait(&kv_empty[st], ph ^ 1u, vabort, p.wait_limit)) {
+          *vabort = 1;
+          break;
+        }
+        tg::mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf) {
+          tg::tma_load_3d(sK + st * C::kTileBytes + hf * 16384, &tm_k, &kv_full[st], hf * 64, kvh,
+                          seq_start + j * kBlockN);
+          tg::tma_load_3d(sV + st * C::kTileBytes + hf * 16384, &tm_v, &kv_full[st], hf * 64, kvh,
+                          seq_start + j * kBlockN);
+        }
+        issued = j + 1;
+      }
+      *n_issued = issued;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc_s = tg::idesc_bf16_f32(kBlockM, kBlockN);        // Q K^T, both K-major
+      const uint32_t idesc_o = tg::idesc_bf16_f32(kBlockM, D, 0, 1);        // P V, V MN-major
+      const uint32_t colS[2] = {C::kColS0, C::kColS1};
+      const uint32_t colO[2] = {C::kColO0, C::kColO1};
+      bool ok = tg::mbar_wait(q_full, 0, vabort, p.wait_limit);
+      int consumed = 0;
+      auto issue_s = [&](int t, int st) {
+        const uint32_t qa = tg::smem_u32(sQ + t * C::kTileBytes);
+        const uint32_t kb = tg::smem_u32(sK + st * C::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          const uint64_t ad = tg::smem_desc(qa + off, 16, 1024, tg::kSwz128);
+          const uint64_t bd = tg::smem_desc(kb + off, 16, 1024, tg::kSwz128);
+          tg::mma_bf16_ss(tmem + colS[t], ad, bd, idesc_s, k != 0);
+        }
+        tg::mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, bool first) {
+        const uint32_t vb = tg::smem_u32(sV + st * C::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < kBlockN / 16; ++k) {
+          // keys 16k..16k+15: 16 rows of 128 B in every d-half; d-halves 16 KB apart
+          const uint64_t bd = tg::smem_desc(vb + k * 2048, 16384, 1024, tg::kSwz128);
+          tg::mma_bf16_ts(tmem + colO[t], tmem + colS[t] + k * 8, bd, idesc_o,
+                          !(first && k == 0));
+        }
+      };
+      if (ok) {
+        if (!tg::mbar_wait(&kv_full[0], 0, vabort, p.wait_limit)) ok = false;
+      }
+      if (ok) {
+        tg::tc_fence_after();
+        for (int t = 0; t < n_tiles; ++t) issue_s(t, 0);
+        // Per step j and tile t: PV_t(j) once P_t(j) is in tensor memory; then S_t(j+1), but
+        // only after PV_t(j) has finished reading P_t(j), whose columns S_t(j+1) overwrites.
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int st = j % C::kStages;
+          const bool has_next = j + 1 < n_kv;
+          const int st_n = (j + 1) % C::kStages;
+          for (int t = 0; t < n_tiles && ok; ++t) {
+            if (!tg::mbar_wait(&p_full[t], j & 1, vabort, p.wait_limit)) {
+              ok = false;
+              break;
+            }
+            tg::tc_fence_after();
+            issue_pv(t, st, j == 0);
+            tg::mma_commit(has_next ? &pv_done[t] : &o_final[t]);
+            if (t == n_tiles - 1) {
+              tg::mma_commit(&kv_empty[st]);
+              consumed = j + 1;
+            }
+            if (has_next) {
+              if (t == 0 &&
+                  !tg::mbar_wait(&kv_full[st_n], ((j + 1) / C::kStages) & 1, vabort,
+                                 p.wait_limit)) {
+                ok = false;
+                break;
+              }
+              if (!tg::mbar_wait(&pv_done[t], j & 1, vabort, p.wait_limit)) {
+                ok = false;
+                break;
+              }
+              tg::tc_fence_after();
+              issue_s(t, st_n);
+            }
+          }
+        }
+      }
+      *n_consumed = consumed;
+      if (!ok) {
+        *vabort = 1;
+        tg::mma_commit(drain);
+        volatile int32_t never = 0;
+        tg::mbar_wait(drain, 0, &never, p.wait_limit);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax / correction / epilogue ----------------
+    const int t = (warp - 4) >> 2;          // Q tile 0 (warps 4-7) or 1 (warps 8-11)
+    const int wq = warp & 3;                 // TMEM lane quarter
+    const int r = wq * 32 + lane;            // query row within the tile
+    const int bar_id = 1 + t;
+    if (t < n_tiles) {
+      const int h = h0 + t;
+      const float scale = p.scale_log2[h];
+      const float beta = p.beta[h];
+      const bool use_bias = (p.g != nullptr) && (beta != 0.0f);
+      const uint32_t colS = t == 0 ? C::kColS0 : C::kColS1;
+      const uint32_t colO = t == 0 ? C::kColO0 : C::kColO1;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+      float *bias_buf = sBias + t * 256;
+      float m_ref = -INFINITY;  // reference max (log2 units)
+      float l = 0.0f;
+      // prefetch this thread's key gate for KV tile 0
+      float g_next = 1.0f;
+      if (use_bias) {
+        const int key = seq_start + r;
+        g_next = (r < seq_len) ? p.g[key] : 1.0f;
+      }
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        // bias of the 128 keys of tile j, shared by the 128 rows of this Q tile
+        float *bias = bias_buf + (j & 1) * 128;
+        if (use_bias) {
+          bias[r] = beta * lg2(g_next);
+          if (j + 1 < n_kv) {
+            const int kr = (j + 1) * kBlockN + r;
+            g_next = (kr < seq_len) ? p.g[seq_start + kr] : 1.0f;
+          }
+        }
+        // the vote is also the barrier that publishes this step's bias to the warpgroup
+        ok = named_bar_and(bar_id, 128, tg::mbar_wait(&s_full[t], j & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        tg::tc_fence_after();
+        uint32_t sr[128];
+        {
+          uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+          uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+          tg::tmem_ld_32x32b_x32(lane_addr + colS + 0, a0);
+          tg::tmem_ld_32x32b_x32(lane_addr + colS + 32, a1);
+          tg::tmem_ld_32x32b_x32(lane_addr + colS + 64, a2);
+          tg::tmem_ld_32x32b_x32(lane_addr + colS + 96, a3);
+          tg::tmem_ld_wait();
+        }
+        // logits in log2 units, causal mask on the diagonal tile
+        const bool diag = (j == tq);
+        float tile_max = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float x = __uint_as_float(sr[c]) * scale;
+          if (use_bias) x += bias[c];
+          if (diag && c > r) x = -INFINITY;
+          sr[c] = __float_as_uint(x);
+          tile_max = fmaxf(tile_max, x);
+        }
+        // lazy max update; rescale O and l only when the max moved by more than the threshold
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (j == 0) {
+          m_ref = tile_max;
+        } else if (tile_max > m_ref + kRescaleThreshold) {
+          alpha = ex2(m_ref - tile_max);
+          m_ref = tile_max;
+          rescale = true;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        float rowsum = 0.0f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float pa = ex2(__uint_as_float(sr[2 * c]) - m_use);
+          const float pb = ex2(__uint_as_float(sr[2 * c + 1]) - m_use);
+          rowsum += pa + pb;
+          pk[c] = tg::pack_bf16x2(pa, pb);
+        }
+        l = l * alpha + rowsum;
+        if (__any_sync(0xFFFFFFFFu, rescale)) {
+          // O_t *= alpha for this row (previous PV into O_t has completed: S_t(j) was issued
+          // after it, and s_full fired only when every earlier MMA had finished)
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
+            tg::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tg::tmem_st_32x32b_x32(lane_addr + colO + c0, o);
+          }
+        }
+        // P (bf16 pairs) over the first 64 columns of S_t
+        {
+          uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+          uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+          tg::tmem_st_32x32b_x32(lane_addr + colS + 0, p0);
+          tg::tmem_st_32x32b_x32(lane_addr + colS + 32, p1);
+        }
+        tg::tmem_st_wait();
+        tg::tc_fence_before();
+        tg::mbar_arrive(&p_full[t]);
+      }
+      // ---- epilogue: O / l -> bf16 rows of O ----
+      if (ok) ok = named_bar_and(bar_id, 128, tg::mbar_wait(&o_final[t], 0, vabort, p.wait_limit));
+      if (ok) {
+        tg::tc_fence_after();
+        const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+        const int row = q0 + r;
+        uint16_t *orow = p.O + (static_cast<size_t>(seq_start + row) * p.H_q + h) * D;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
+          tg::tmem_ld_wait();
+          if (row < seq_len) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = tg::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                     __uint_as_float(o[2 * i + 1]) * inv_l);
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      } else {
+        *vabort = 1;
+      }
+    }
+  }
+
+  tg::tc_fence_before();
+  __syncthreads();
+  if (*vabort) {
+    if (threadIdx.x == 0) {
+      tg::report(p.status, TG_DEV_TIMEOUT);
+      volatile int32_t never = 0;
+      for (int i = *n_consumed; i < *n_issued; ++i)
+        tg::mbar_wait(&kv_full[i % C::kStages], (i / C::kStages) & 1, &never, p.wait_limit);
+      tg::mbar_wait(q_full, 0, &never, p.wait_limit);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tg::tc_fence_after();
+    tg::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                             AttnParams &p, cudaStream_t stream) {
+  using C = AttnCfg<D>;
+  CUtensorMap tm_q, tm_k, tm_v;
+  const uint32_t box[3] = {64, 1, 128};
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(p.H_q),
+                              static_cast<uint64_t>(p.M_cap)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(p.H_q) * D * 2};
+    if (!tg_host::encode_tmap_bf16(&tm_q, Q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TG_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(p.H_kv),
+                              static_cast<uint64_t>(p.M_cap)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(p.H_kv) * D * 2};
+    if (!tg_host::encode_tmap_bf16(&tm_k, K, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TG_ERR_CUDA;
+    if (!tg_host::encode_tmap_bf16(&tm_v, V, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TG_ERR_CUDA;
+  }
+  cudaError_t e = cudaFuncSetAttribute(gated_attention_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return tg_host::record_cuda(e);
+  const long long grid = static_cast<long long>(p.n_qt_max) * p.B * p.pairs;
+  if (grid == 0) return TG_OK;
+  if (grid > 0x7FFFFFFFLL) return TG_ERR_UNSUPPORTED;
+  gated_attention_kernel<D><<<static_cast<int>(grid), kThreads, C::kSmemBytes, stream>>>(
+      tm_q, tm_k, tm_v, p);
+  return tg_host::record_cuda(cudaGetLastError());
+}
+
+}  // namespace
+
+namespace tg_host {
+
+tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                 int32_t *status, cudaStream_t stream) {
+  if (M_cap == 0 || max_seqlen == 0) return TG_OK;
+  AttnParams p;
+  p.g = g;
+  p.cu_kept = cu_kept;
+  p.B = B;
+  p.M_cap = M_cap;
+  p.max_seqlen = max_seqlen;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.group = H_q / H_kv;
+  p.heads_per_cta = (p.group % 2 == 0) ? 2 : 1;
+  p.pairs = H_q / p.heads_per_cta;
+  p.n_qt_max = (max_seqlen + kBlockM - 1) / kBlockM;
+  p.O = O;
+  p.status = status;
+  p.wait_limit = wait_limit_ns();
+  const float log2e = 1.4426950408889634f;
+  for (int h = 0; h < kMaxHeads; ++h) {
+    p.scale_log2[h] = h < H_q ? tau[h] * log2e / std::sqrt(static_cast<float>(d_h)) : 0.0f;
+    p.beta[h] = h < H_q ? beta[h] : 0.0f;
+  }
+  if (d_h == 128) return launch_attention_d<128>(Q, K, V, p, stream);
+  if (d_h == 64) return launch_attention_d<64>(Q, K, V, p, stream);
+  return TG_ERR_UNSUPPORTED;
+}
+
+}  // namespace tg_host

@@ -1,0 +1,91 @@
+"""The C-ABI library: it loads without a GPU, exports every entry point the header declares,
+and rejects bad host arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from learned_token_pruning_07_b300 import binding, build
+
+pytestmark = pytest.mark.cpu
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tokengate.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.tg_version() == 100
+    assert lib.tg_status_string(binding.TG_OK) == b"ok"
+    assert b"capacity" in lib.tg_status_string(binding.TG_ERR_CAPACITY)
+
+
+FAKE = 0x1000  # never dereferenced: every call below fails validation first
+
+
+def test_gate_score_rejects_bad_arguments(lib):
+    f = lib.tg_gate_score
+    assert f(None, 8, 256, None, FAKE, None, FAKE, 0.0, 64, FAKE, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, -1, 256, None, FAKE, None, FAKE, 0.0, 64, FAKE, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, 8, 250, None, FAKE, None, FAKE, 0.0, 64, FAKE, None, None, None) == binding.TG_ERR_UNSUPPORTED
+    assert f(FAKE, 8, 256, None, FAKE, None, FAKE, 0.0, 1024, FAKE, None, None, None) == binding.TG_ERR_UNSUPPORTED
+    assert f(FAKE + 2, 8, 256, None, FAKE, None, FAKE, 0.0, 64, FAKE, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, 8, 256, None, FAKE, None, FAKE, float("nan"), 64, FAKE, None, None, None) == binding.TG_ERR_INVALID_ARG
+
+
+def test_select_rejects_bad_arguments(lib):
+    f = lib.tg_topk_select
+    assert f(FAKE, None, FAKE, 1, 10, -1, FAKE, 10, FAKE, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, FAKE, 0, 10, 3, FAKE, 10, FAKE, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, FAKE, 1, 10, 3, None, 10, FAKE, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, FAKE, 5000, 10, 3, FAKE, 10, FAKE, None, None) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_gather_rejects_bad_arguments(lib):
+    f = lib.tg_gather_kept
+    assert f(FAKE, None, None, FAKE, 1, 10, 12, FAKE, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, None, FAKE, 1, 10, 16, None, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+
+
+def test_attention_rejects_bad_arguments(lib):
+    f = lib.tg_gated_attention
+    tau = np.ones(4, np.float32)
+    beta = np.ones(4, np.float32)
+    bad_tau = np.array([1, 0, 1, 1], np.float32)
+    neg_beta = np.array([1, -1, 1, 1], np.float32)
+    args = lambda t, b, hq=4, hkv=2, dh=64: (FAKE, FAKE, FAKE, None, FAKE, 1, 64, 64, hq, hkv, dh,
+                                             t.ctypes.data, b.ctypes.data, FAKE, None, None)
+    assert f(*args(bad_tau, beta)) == binding.TG_ERR_INVALID_ARG
+    assert f(*args(tau, neg_beta)) == binding.TG_ERR_INVALID_ARG
+    assert f(*args(tau, beta, hq=4, hkv=3)) == binding.TG_ERR_UNSUPPORTED
+    assert f(*args(tau, beta, dh=96)) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_rope_rejects_bad_arguments(lib):
+    f = lib.tg_apply_rope
+    assert f(FAKE, FAKE, None, 0, 10, 2, 63, 1e6, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, None, 0, 10, 2, 64, -1.0, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, None, 0, 10, 2, 512, 1e6, None) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_wait_limit_setter(lib):
+    assert lib.tg_set_wait_limit_ns(1000) == binding.TG_OK
+    assert lib.tg_set_wait_limit_ns(0) == binding.TG_OK

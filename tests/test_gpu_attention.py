@@ -1,0 +1,110 @@
+"""GPU parity: token-gated causal GQA attention (tcgen05) against the fp64 oracle.
+
+Bar: 2e-2 max-abs and 1e-2 mean-relative error, bf16 output against fp64."""
+import numpy as np
+import pytest
+import torch
+
+from learned_token_pruning_07_b300 import binding as tg
+from learned_token_pruning_07_b300 import inputs as I
+from oracle import tokengate_oracle as O
+from tests._helpers import (ATTN_MAX_ABS, ATTN_MEAN_REL, attention_close, bf16_dev_to_f64, dev, host,
+                            sampled_rows, status_word)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, lens, tag=0, use_g=True, beta_zero=False, rows=None, capacity=None, g_override=None):
+    cu = I.cu_seqlens_of(lens)
+    M = int(cu[-1])
+    at = I.make_attention_inputs(wl, M, tag_extra=tag)
+    g = at["g"] if g_override is None else g_override
+    tau, beta = at["tau"], at["beta"]
+    if beta_zero:
+        beta = np.zeros_like(beta)
+    cap = M if capacity is None else capacity
+    Qd, Kd, Vd = dev(at["Q"]), dev(at["K"]), dev(at["V"])
+    O_d = torch.full((M, wl.H_q, wl.d_h), 0x7FC0, dtype=torch.int16, device="cuda")  # NaN fill
+    st = status_word()
+    tg.gated_attention(Qd[:cap], Kd[:cap], Vd[:cap], dev(cu), tau, beta, O_d[:cap],
+                       max_seqlen=max(lens) if lens else 0, g=dev(g) if use_g else None, status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    got = bf16_dev_to_f64(O_d)
+    ref = O.gated_attention(I.bf16_bits_to_f64(at["Q"]), I.bf16_bits_to_f64(at["K"]),
+                            I.bf16_bits_to_f64(at["V"]), g.astype(np.float64) if use_g else None,
+                            cu, tau.astype(np.float64), beta.astype(np.float64), rows=rows)
+    return got if rows is None else got[rows], ref
+
+
+def _assert_close(got, ref):
+    mx, mr = attention_close(got, ref)
+    assert np.all(np.isfinite(got))
+    assert mx <= ATTN_MAX_ABS and mr <= ATTN_MEAN_REL, (mx, mr)
+
+
+def test_attention_tiny_dh64():
+    wl = I.WORKLOADS["tiny"]
+    _assert_close(*_run(wl, [96]))
+
+
+@pytest.mark.parametrize("lens", [[1], [127], [128], [129], [300, 1, 45, 256], [0, 200, 0]])
+def test_attention_varlen_dh128(lens):
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    _assert_close(*_run(wl, lens, tag=len(lens)))
+
+
+def test_attention_qwen3_8k_full():
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    _assert_close(*_run(wl, [1152]))
+
+
+def test_attention_beta_zero_and_no_gate_are_plain_causal():
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    a_got, a_ref = _run(wl, [400], beta_zero=True)
+    b_got, b_ref = _run(wl, [400], use_g=False)
+    _assert_close(a_got, a_ref)
+    _assert_close(b_got, b_ref)
+    np.testing.assert_allclose(a_ref, b_ref, rtol=0, atol=1e-12)
+
+
+def test_attention_strong_gates_and_zero_gates():
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    M = 260
+    g = np.random.default_rng(3).uniform(1e-6, 1.0, M).astype(np.float32)
+    g[::5] = 1e-30
+    _assert_close(*_run(wl, [M], g_override=g))
+    g0 = np.zeros(M, np.float32)
+    got, ref = _run(wl, [M], g_override=g0)          # every key has zero weight -> zeros
+    assert np.all(ref == 0.0) and np.all(got == 0.0)
+
+
+def test_attention_odd_group_one_head_per_cta():
+    wl = I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=6, H_kv=2)   # group of 3
+    _assert_close(*_run(wl, [333]))
+
+
+def test_attention_mha_group_of_one():
+    wl = I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=4, H_kv=4)
+    _assert_close(*_run(wl, [200, 70]))
+
+
+def test_attention_sweep_k4096_full():
+    wl = I.WORKLOADS["sweep_32k"]
+    _assert_close(*_run(wl, [4096 + 256]))
+
+
+def test_attention_sweep_k16384_sampled_rows():
+    wl = I.WORKLOADS["sweep_32k"]
+    M = 16384 + 256
+    cu = I.cu_seqlens_of([M])
+    rows = sampled_rows(cu, list(range(M - 256, M)), 700, seed=5)
+    _assert_close(*_run(wl, [M], rows=rows))
+
+
+def test_attention_ragged_batch_sampled_rows():
+    wl = I.WORKLOADS["ragged_b8"]
+    lens = [min(2048, d) + n for d, n in zip(wl.doc_lens, wl.instr_lens)]
+    cu = I.cu_seqlens_of(lens)
+    rows = sampled_rows(cu, [], 600, seed=6)
+    _assert_close(*_run(wl, lens, rows=rows))

@@ -1,0 +1,66 @@
+"""GPU parity: gate scoring (tcgen05 GEMM + fused SiLU . w2 + sigmoid) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from learned_token_pruning_07_b300 import binding as tg
+from learned_token_pruning_07_b300 import inputs as I
+from oracle import tokengate_oracle as O
+from tests._helpers import G_ATOL, S_ATOL, S_RTOL, dev, host, status_word
+
+pytestmark = pytest.mark.gpu
+
+
+def _score(wl, rows=None, b1=None, b2=0.0, with_mask=True):
+    gi = I.make_gate_inputs(wl)
+    T = wl.T_total
+    s = torch.full((T + 32,), 12345.0, dtype=torch.float32, device="cuda")
+    g = torch.full((T + 32,), 12345.0, dtype=torch.float32, device="cuda")
+    st = status_word()
+    mask = gi["instr_mask"] if with_mask else np.zeros(T, np.uint8)
+    tg.gate_score(dev(gi["h"]), dev(gi["W1"]), dev(gi["w2"]), s[:T], g[:T],
+                  instr_mask=dev(mask) if with_mask else None,
+                  b1=None if b1 is None else dev(b1.astype(np.float32)), b2=b2, status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    s_h, g_h = host(s), host(g)
+    assert np.all(s_h[T:] == 12345.0) and np.all(g_h[T:] == 12345.0)  # nothing past T
+    h64 = I.bf16_bits_to_f64(gi["h"] if rows is None else gi["h"][rows])
+    m = mask if rows is None else mask[rows]
+    ref_s, ref_g = O.gate_score(h64, I.bf16_bits_to_f64(gi["W1"]), I.bf16_bits_to_f64(gi["w2"]), m,
+                                None if b1 is None else b1.astype(np.float32).astype(np.float64), b2)
+    got_s = s_h[:T] if rows is None else s_h[rows]
+    got_g = g_h[:T] if rows is None else g_h[rows]
+    np.testing.assert_allclose(got_s, ref_s, rtol=S_RTOL, atol=S_ATOL)
+    np.testing.assert_allclose(got_g, ref_g, rtol=0, atol=G_ATOL)
+    return got_s, ref_s
+
+
+def test_score_tiny():
+    _score(I.WORKLOADS["tiny"])
+
+
+def test_score_ragged_tail_and_bias():
+    # T not a multiple of the 128-row tile; d_g = 384 splits into two 192-wide MMAs
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(900,), instr_lens=(17,), d=512, d_g=384)
+    b1 = np.random.default_rng(4).standard_normal(384) * 0.5
+    _score(wl, b1=b1, b2=-0.25)
+
+
+def test_score_small_dg_no_mask():
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(130,), instr_lens=(0,), d=64, d_g=32)
+    _score(wl, with_mask=False)
+
+
+def test_score_qwen3_gate_layer_8k():
+    got, ref = _score(I.WORKLOADS["qwen3_1p7b_8k"])
+    # the score error is far below the spread of the scores, so top-K sees the same order
+    assert np.max(np.abs(got - ref)) < 1e-3 * np.std(ref) + 1e-4
+
+
+def test_score_full_size_sweep_sampled_rows():
+    wl = I.WORKLOADS["sweep_32k"]
+    rng = np.random.default_rng(21)
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(wl.T_total - 300, wl.T_total),
+                                     rng.integers(0, wl.T_total, 2000)]))
+    _score(wl, rows=rows)
