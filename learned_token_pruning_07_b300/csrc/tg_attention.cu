@@ -13,11 +13,15 @@
 // Warp roles (12 warps):
 //   warp 0       TMA producer: Q tiles once, then the K/V ring (kStages deep)
 //   warp 1       tensor-memory owner and MMA issuer:  S_t = Q_t K^T ; O_t += P_t V
+//   warp 2       bias producer: beta_h * log2(g_j) of each K/V tile's 128 keys, both heads,
+//                into a shared-memory ring that follows the K/V stages
 //   warps 4-7    softmax + correction + epilogue for Q tile 0 (thread = query row = TMEM lane)
 //   warps 8-11   the same for Q tile 1
 // Online softmax with a lazily updated running max: the reference max m only moves when the
 // tile max exceeds it by more than 8 (log2 units), so the O rescale (a TMEM read-modify-write)
-// is rare; the result is exact either way because O and l share the same reference.
+// is rare; the result is exact either way because O and l share the same reference. The
+// softmax runs on packed fp32 pairs (fma/add .f32x2) with 3-input max, and only the diagonal
+// key tile carries the causal mask.
 #include "tg_common.cuh"
 
 namespace {
@@ -36,8 +40,8 @@ struct AttnCfg {
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = 2 * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-  static constexpr uint32_t kOffBias = kOffV + kStages * kTileBytes;       // [2 tiles][2][128] f32
-  static constexpr uint32_t kOffBar = kOffBias + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kOffBias = kOffV + kStages * kTileBytes;       // [stage][2 heads][128] f32
+  static constexpr uint32_t kOffBar = kOffBias + kStages * 2 * 128 * 4;
   static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 };
@@ -65,19 +69,34 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Barrier over the `n` threads of named barrier `id` that also ANDs a predicate across them,
-// so a give-up decision is taken by the whole warpgroup at once.
-__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
+// Packed fp32 pairs (Blackwell .f32x2 arithmetic).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 template <int D>
@@ -102,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *p_full = s_full + 2;             // [2]
   uint64_t *o_final = p_full + 2;            // [2]
   uint64_t *pv_done = o_final + 2;           // [2]
-  uint64_t *drain = pv_done + 2;
+  uint64_t *bias_full = pv_done + 2;         // [kStages]
+  uint64_t *drain = bias_full + C::kStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
@@ -139,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       tg::mbar_init(&kv_full[i], 1);
       tg::mbar_init(&kv_empty[i], 1);
+      tg::mbar_init(&bias_full[i], 32);
     }
     for (int t = 0; t < 2; ++t) {
       tg::mbar_init(&s_full[t], 1);
@@ -271,42 +292,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::mbar_wait(drain, 0, &never, p.wait_limit);
       }
     }
+  } else if (warp == 2) {
+    // ---------------- bias producer: beta_h * log2(g) per key, both heads ----------------
+    if (p.g != nullptr) {
+      const float beta0 = p.beta[h0];
+      const float beta1 = n_tiles > 1 ? p.beta[h0 + 1] : 0.0f;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        // the stage is free once both tiles' PV of step j - kStages has completed (the same
+        // barrier that frees the K/V stage); by then both softmax warpgroups are done with it
+        if (!tg::mbar_wait(&kv_empty[st], ph ^ 1u, vabort, p.wait_limit)) {
+          *vabort = 1;
+          break;
+        }
+        float *dst = sBias + st * 256;
+        float gv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = j * kBlockN + lane * 4 + i;
+          gv[i] = k < seq_len ? p.g[seq_start + k] : 1.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lgv = lg2(gv[i]);
+          dst[lane * 4 + i] = beta0 == 0.0f ? 0.0f : beta0 * lgv;
+          dst[128 + lane * 4 + i] = beta1 == 0.0f ? 0.0f : beta1 * lgv;
+        }
+        tg::mbar_arrive(&bias_full[st]);
+      }
+    }
   } else if (warp >= 4) {
     // ---------------- softmax / correction / epilogue ----------------
     const int t = (warp - 4) >> 2;          // Q tile 0 (warps 4-7) or 1 (warps 8-11)
     const int wq = warp & 3;                 // TMEM lane quarter
     const int r = wq * 32 + lane;            // query row within the tile
-    const int bar_id = 1 + t;
     if (t < n_tiles) {
       const int h = h0 + t;
       const float scale = p.scale_log2[h];
-      const float beta = p.beta[h];
-      const bool use_bias = (p.g != nullptr) && (beta != 0.0f);
+      const bool use_bias = p.g != nullptr;  // beta = 0 arrives as a zero bias
       const uint32_t colS = t == 0 ? C::kColS0 : C::kColS1;
       const uint32_t colO = t == 0 ? C::kColO0 : C::kColO1;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-      float *bias_buf = sBias + t * 256;
+      const uint64_t scale2 = f2(scale, scale);
       float m_ref = -INFINITY;  // reference max (log2 units)
       float l = 0.0f;
-      // prefetch this thread's key gate for KV tile 0
-      float g_next = 1.0f;
-      if (use_bias) {
-        const int key = seq_start + r;
-        g_next = (r < seq_len) ? p.g[key] : 1.0f;
-      }
       bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
-        // bias of the 128 keys of tile j, shared by the 128 rows of this Q tile
-        float *bias = bias_buf + (j & 1) * 128;
-        if (use_bias) {
-          bias[r] = beta * lg2(g_next);
-          if (j + 1 < n_kv) {
-            const int kr = (j + 1) * kBlockN + r;
-            g_next = (kr < seq_len) ? p.g[seq_start + kr] : 1.0f;
-          }
-        }
-        // the vote is also the barrier that publishes this step's bias to the warpgroup
-        ok = named_bar_and(bar_id, 128, tg::mbar_wait(&s_full[t], j & 1, vabort, p.wait_limit));
+        const int st = j % C::kStages;
+        bool w = tg::mbar_wait(&s_full[t], j & 1, vabort, p.wait_limit);
+        if (use_bias) w = w && tg::mbar_wait(&bias_full[st], (j / C::kStages) & 1, vabort, p.wait_limit);
+        ok = __all_sync(0xFFFFFFFFu, w);  // tcgen05.ld below is warp-collective
         if (!ok) break;
         tg::tc_fence_after();
         uint32_t sr[128];
@@ -321,16 +357,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tg::tmem_ld_32x32b_x32(lane_addr + colS + 96, a3);
           tg::tmem_ld_wait();
         }
-        // logits in log2 units, causal mask on the diagonal tile
-        const bool diag = (j == tq);
-        float tile_max = -INFINITY;
+        // logits in log2 units: x = s * scale + bias (pairs)
+        uint64_t x2[64];
+        if (use_bias) {
+          const float4 *bias4 = reinterpret_cast<const float4 *>(sBias + st * 256 + t * 128);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float x = __uint_as_float(sr[c]) * scale;
-          if (use_bias) x += bias[c];
-          if (diag && c > r) x = -INFINITY;
-          sr[c] = __float_as_uint(x);
-          tile_max = fmaxf(tile_max, x);
+          for (int c = 0; c < 32; ++c) {
+            const float4 bv = bias4[c];
+            x2[2 * c] = f2_fma(f2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), scale2,
+                               f2(bv.x, bv.y));
+            x2[2 * c + 1] = f2_fma(f2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])),
+                                   scale2, f2(bv.z, bv.w));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            x2[c] = f2_mul(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2);
+        }
+        float tile_max = -INFINITY;
+        if (j == tq) {
+          // diagonal tile: key c is visible to row r only when c <= r
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            float a, bb;
+            f2_split(x2[c], a, bb);
+            a = (2 * c > r) ? -INFINITY : a;
+            bb = (2 * c + 1 > r) ? -INFINITY : bb;
+            x2[c] = f2(a, bb);
+            tile_max = fmax3(tile_max, a, bb);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            float a, bb;
+            f2_split(x2[c], a, bb);
+            tile_max = fmax3(tile_max, a, bb);
+          }
         }
         // lazy max update; rescale O and l only when the max moved by more than the threshold
         float alpha = 1.0f;
@@ -343,19 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-        float rowsum = 0.0f;
+        const uint64_t negm2 = f2(-m_use, -m_use);
+        uint64_t sum2 = f2(0.0f, 0.0f);
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float pa = ex2(__uint_as_float(sr[2 * c]) - m_use);
-          const float pb = ex2(__uint_as_float(sr[2 * c + 1]) - m_use);
-          rowsum += pa + pb;
+          float a, bb;
+          f2_split(f2_add(x2[c], negm2), a, bb);
+          const float pa = ex2(a), pb = ex2(bb);
+          sum2 = f2_add(sum2, f2(pa, pb));
           pk[c] = tg::pack_bf16x2(pa, pb);
         }
-        l = l * alpha + rowsum;
+        float s_lo, s_hi;
+        f2_split(sum2, s_lo, s_hi);
+        l = l * alpha + (s_lo + s_hi);
         if (__any_sync(0xFFFFFFFFu, rescale)) {
-          // O_t *= alpha for this row (previous PV into O_t has completed: S_t(j) was issued
-          // after it, and s_full fired only when every earlier MMA had finished)
+          // O_t *= alpha for this row (the PV of step j-1 into O_t has completed: S_t(j) was
+          // issued after it, and s_full fired only when every earlier MMA had finished)
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
@@ -377,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::mbar_arrive(&p_full[t]);
       }
       // ---- epilogue: O / l -> bf16 rows of O ----
-      if (ok) ok = named_bar_and(bar_id, 128, tg::mbar_wait(&o_final[t], 0, vabort, p.wait_limit));
+      if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&o_final[t], 0, vabort, p.wait_limit));
       if (ok) {
         tg::tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
