@@ -36,7 +36,7 @@ import numpy as np  # noqa: E402
 METRIC = "gated-prefill tokens/s (score+topK+gather+gated attn), N=32K; % of roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
 
 # ---------------------------------------------------------------------------
@@ -117,13 +117,13 @@ def measured_traffic(kernel: str, workload: str, K: int):
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
-        j = json.load(f)
-    e = j.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash(kernel):
-        return None
-    if e.get("workload") != workload or int(e.get("K", -1)) != K:
-        return None
-    return float(e["dram_bytes_per_launch"])
+        for line in f:
+            parts = line.split()
+            if len(parts) != 5 or line.startswith("#") or parts[0] != kernel:
+                continue
+            if parts[1] == workload and int(parts[2]) == K and parts[3] == kernel_source_hash(kernel):
+                return float(parts[4])
+    return None
 
 
 # ---------------------------------------------------------------------------
