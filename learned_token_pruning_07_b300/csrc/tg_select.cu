@@ -7,8 +7,11 @@
 // keys (instruction rows -> 0, never selected as documents; NaN -> 1, below every number;
 // -0.0 -> +0.0). The K_b-th largest document key is found by an MSB-first radix select in
 // three passes of 11, 11 and 10 bits: each CTA builds a 2048-bin histogram of its chunk in
-// shared memory with warp-aggregated atomics (__match_any_sync), the cluster sums the eight
-// histograms through distributed shared memory, and every CTA picks the same bin. After the
+// shared memory with shared atomics and sums it into 64 coarse bins of 32; after a cluster
+// barrier every CTA reads the eight coarse histograms through distributed shared memory,
+// picks the coarse bin holding the wanted rank, then reads only that coarse bin's 32 fine
+// bins from the eight CTAs (two small remote rounds instead of pulling whole histograms,
+// since DSMEM bandwidth, not latency, dominated), and every CTA picks the same digit. After the
 // third pass the threshold key T and the number of ties at T to keep are exact; ties are
 // granted to the lowest indices. Compaction: each warp owns a contiguous segment of its
 // CTA's chunk; per-warp counts of keys above / at T and of instruction rows, one DSMEM
@@ -23,18 +26,23 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCluster = 8;
 constexpr int kMaxB = 1024;
-constexpr int kBins = 2048;
+constexpr int kBins = 2048;  // 11-bit digits
+constexpr int kFine = 32;    // fine bins per coarse bin
+constexpr int kCoarse = kBins / kFine;
 constexpr int kMaxSmemKeys = 40960;  // 160 KB; longer chunks stream their keys from L2
+static_assert(kBins == 4 * kThreads, "each thread owns four histogram bins");
+static_assert(kCoarse * kCluster == kThreads, "one thread per (coarse bin, rank)");
 
 struct SelectParams {
   const float *s;
   const uint8_t *mask;
   const int32_t *cu_seqlens;
   int32_t B, T, K, capacity, smem_keys;
+  int32_t vec;  // s is 16-byte and mask 4-byte aligned: stage keys with vector loads
   int32_t *kept_idx;
   int32_t *cu_kept;
   int32_t *status;
@@ -54,14 +62,73 @@ __device__ __forceinline__ uint32_t load_key(const SelectParams &p, int j) {
   return m ? 0u : order_key(v);
 }
 
+// Cluster barrier halves: arrive publishes this thread's earlier shared-memory writes to
+// the cluster, wait makes every other CTA's writes before its arrive visible here.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Load a 32-bit word from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ int32_t ld_peer(const int32_t *local_addr, int rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local_addr)), r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(r) : "memory");
+  return v;
+}
+__device__ __forceinline__ int4 ld_peer4(const int4 *local_addr, int rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local_addr)), r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(r)
+               : "memory");
+  return v;
+}
+
+// Sum over the 8 consecutive lanes of a lane group (lane & ~7 .. lane | 7).
+__device__ __forceinline__ int sum8(int v) {
+  v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+  v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+  v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+  return v;
+}
+
+// Inclusive suffix sum over the lanes of a warp (lane l gets the sum of lanes l..31).
+__device__ __forceinline__ int warp_suffix(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_down_sync(0xFFFFFFFFu, v, o);
+    if (lane + o < 32) v += t;
+  }
+  return v;
+}
+
 struct SelShared {
-  int32_t hist[2][kBins];
-  int32_t warp_tot[kWarps];
+  int32_t hist[2][kBins];     // fine histogram, double-buffered by pass parity
+  int32_t coarse[2][kCoarse]; // sums of 32 consecutive fine bins, same buffering
+  int32_t ctot[kCoarse];      // cluster-wide coarse totals
+  int32_t ftot[kFine];        // cluster-wide counts of the fine bins inside the chosen coarse bin
+  int32_t pick[4][4];         // per pass: coarse bin, keys needed in it, digit, keys needed in it
+  int32_t n_need;             // keys the selection takes: min(K, document rows)
   int32_t wgt[kWarps], weq[kWarps], wnm[kWarps];
   int32_t woff[kWarps], wtie[kWarps];
-  int32_t xch[4];  // this CTA's counts: [0] keys > T, [1] keys == T, [2] instruction rows
-  int32_t bcast[4];
-  int32_t prev_cnt[kMaxB];
+  int32_t red[kWarps];
+  int4 xch;                 // this CTA's counts: keys > T, keys == T, instruction rows
+  int32_t m_b;              // the sequence's end offset in the kept list
+  int32_t prev_cnt[kMaxB];  // instruction rows of each earlier sequence inside this chunk
 };
 
 // Block-wide sum of one int per thread (valid in every thread).
@@ -69,23 +136,18 @@ __device__ __forceinline__ int block_sum(int v, SelShared &sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  if (lane == 0) sh.warp_tot[warp] = v;
+  if (lane == 0) sh.red[warp] = v;
   __syncthreads();
-  if (warp == 0) {
-    int x = sh.warp_tot[lane];
+  int r = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-    if (lane == 0) sh.bcast[2] = x;
-  }
-  __syncthreads();
-  const int r = sh.bcast[2];
+  for (int w = 0; w < kWarps; ++w) r += sh.red[w];
   __syncthreads();
   return r;
 }
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     topk_select_kernel(SelectParams p) {
-  __shared__ SelShared sh;
+  __shared__ __align__(16) SelShared sh;
   extern __shared__ uint32_t ks[];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -111,7 +173,36 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- stage keys in shared memory; count instruction rows of earlier sequences ----
   for (int i = tid; i < b; i += kThreads) sh.prev_cnt[i] = 0;
-  if (in_smem) {
+  if (in_smem && p.vec) {
+    // aligned body with 16-byte score / 4-byte mask loads, scalar head and tail
+    const int e = lo + len;
+    const int a4 = min(e, (lo + 3) & ~3);
+    const int e4 = max(a4, e & ~3);
+    for (int j = lo + tid; j < a4; j += kThreads) ks[j - lo] = load_key(p, j);
+    for (int j = e4 + tid; j < e; j += kThreads) ks[j - lo] = load_key(p, j);
+    const int nv = (e4 - a4) >> 2;
+    const float4 *s4 = reinterpret_cast<const float4 *>(p.s + a4);
+    const uchar4 *m4 = reinterpret_cast<const uchar4 *>(p.mask + a4);
+    uint32_t *dst = ks + (a4 - lo);
+    for (int v = tid; v < nv; v += 2 * kThreads) {
+      const bool two = v + kThreads < nv;
+      const float4 x0 = s4[v];
+      const float4 x1 = two ? s4[v + kThreads] : x0;
+      const uchar4 q0 = p.mask ? m4[v] : make_uchar4(0, 0, 0, 0);
+      const uchar4 q1 = (p.mask && two) ? m4[v + kThreads] : make_uchar4(0, 0, 0, 0);
+      dst[4 * v + 0] = q0.x ? 0u : order_key(x0.x);
+      dst[4 * v + 1] = q0.y ? 0u : order_key(x0.y);
+      dst[4 * v + 2] = q0.z ? 0u : order_key(x0.z);
+      dst[4 * v + 3] = q0.w ? 0u : order_key(x0.w);
+      if (two) {
+        uint32_t *d1 = dst + 4 * (v + kThreads);
+        d1[0] = q1.x ? 0u : order_key(x1.x);
+        d1[1] = q1.y ? 0u : order_key(x1.y);
+        d1[2] = q1.z ? 0u : order_key(x1.z);
+        d1[3] = q1.w ? 0u : order_key(x1.w);
+      }
+    }
+  } else if (in_smem) {
     int i = tid;
     for (; i + 3 * kThreads < len; i += 4 * kThreads) {
       const uint32_t k0 = load_key(p, lo + i), k1 = load_key(p, lo + i + kThreads);
@@ -146,83 +237,83 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   bool select_none = false;
   for (int pass = 0; pass < 3; ++pass) {
     int32_t *hist = sh.hist[pass & 1];
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+    reinterpret_cast<int4 *>(hist)[tid] = make_int4(0, 0, 0, 0);
     __syncthreads();
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int width = pass < 2 ? 11 : 10;
     const uint32_t dmask = (1u << width) - 1u;
-    for (int base = 0; base < len; base += kThreads) {
-      const int i = base + tid;
-      int bin = -1;
-      if (i < len) {
-        const uint32_t key = key_at(i);
-        if (key != 0u && (pass == 0 || (key >> (shift + width)) == prefix))
-          bin = static_cast<int>((key >> shift) & dmask);
-      }
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
-      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+    for (int i = tid; i < len; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if (key != 0u && (pass == 0 || (key >> (shift + width)) == prefix))
+        atomicAdd(&hist[(key >> shift) & dmask], 1);
     }
-    cluster.sync();
-    if (pass == 0) {
+    __syncthreads();
+    {
+      // local coarse histogram: thread t sums fine bins 4t..4t+3; 8 lanes make a coarse bin
+      const int4 f = reinterpret_cast<const int4 *>(hist)[tid];
+      const int c8 = sum8(f.x + f.y + f.z + f.w);
+      if ((lane & 7) == 0) sh.coarse[pass & 1][tid >> 3] = c8;
+    }
+    cluster_sync_all();
+    if (pass == 0 && b > 0) {
       // earlier sequences: sum of min(n_i, K + |N_i|) = sum of (K_i + |N_i|)
       int part = 0;
       for (int i = tid; i < b; i += kThreads) {
         int c = 0;
-        for (int r = 0; r < kCluster; ++r) c += cluster.map_shared_rank(&sh, r)->prev_cnt[i];
+        for (int r = 0; r < kCluster; ++r) c += ld_peer(&sh.prev_cnt[i], r);
         part += min(p.cu_seqlens[i + 1] - p.cu_seqlens[i], p.K + c);
       }
       seq_offset = block_sum(part, sh);
     }
-    // cluster-wide histogram; thread t owns bins 2047-2t and 2046-2t (descending order)
-    const int bin_hi = kBins - 1 - 2 * tid, bin_lo = bin_hi - 1;
-    int c_hi = 0, c_lo = 0;
-#pragma unroll
-    for (int r = 0; r < kCluster; ++r) {
-      const int32_t *h = cluster.map_shared_rank(hist, r);
-      c_hi += h[bin_hi];
-      c_lo += h[bin_lo];
+    // round 1: cluster-wide coarse totals; thread t reads coarse bin t/8 of rank t%8
+    {
+      const int ct = sum8(ld_peer(&sh.coarse[pass & 1][tid >> 3], tid & 7));
+      if ((lane & 7) == 0) sh.ctot[tid >> 3] = ct;
     }
-    if (pass == 0) {
-      const int n_doc = block_sum(c_hi + c_lo, sh);
-      need = min(p.K, n_doc);
-      if (need == 0) {
-        select_none = true;
-        break;  // uniform: every CTA of the cluster sees the same n_doc
-      }
-    }
-    // inclusive scan of (c_hi + c_lo) over threads = keys in bins >= bin_lo
-    int incl = c_hi + c_lo;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) sh.warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      const int v = sh.warp_tot[lane];
-      int x = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += t;
+      // lane l owns coarse bins 2l and 2l+1; find the one holding the need-th largest key
+      const int lo_c = sh.ctot[2 * lane], hi_c = sh.ctot[2 * lane + 1];
+      const int suf = warp_suffix(lo_c + hi_c);
+      const int all = __shfl_sync(0xFFFFFFFFu, suf, 0);
+      const int nd = pass == 0 ? min(p.K, all) : need;
+      if (lane == 0 && pass == 0) sh.n_need = nd;
+      const int above = suf - lo_c - hi_c;
+      if (above < nd && nd <= above + hi_c) {
+        sh.pick[pass][0] = 2 * lane + 1;
+        sh.pick[pass][1] = nd - above;
+      } else if (above + hi_c < nd && nd <= above + hi_c + lo_c) {
+        sh.pick[pass][0] = 2 * lane;
+        sh.pick[pass][1] = nd - above - hi_c;
       }
-      sh.wgt[lane] = x - v;  // exclusive prefix of warp totals (scratch)
     }
     __syncthreads();
-    incl += sh.wgt[warp];
-    const int above_hi = incl - c_hi - c_lo;  // keys in bins > bin_hi
-    if (above_hi < need && need <= above_hi + c_hi) {
-      sh.bcast[0] = bin_hi;
-      sh.bcast[1] = need - above_hi;
-    } else if (above_hi + c_hi < need && need <= incl) {
-      sh.bcast[0] = bin_lo;
-      sh.bcast[1] = need - above_hi - c_hi;
+    if (pass == 0) {
+      need = sh.n_need;
+      if (need == 0) {
+        select_none = true;
+        break;  // uniform: every CTA of the cluster sees the same count
+      }
+    }
+    // round 2: cluster-wide counts of the 32 fine bins inside the chosen coarse bin
+    const int cbin = sh.pick[pass][0];
+    if (tid < kFine * kCluster) {
+      const int ft = sum8(ld_peer(&hist[cbin * kFine + (tid >> 3)], tid & 7));
+      if ((lane & 7) == 0) sh.ftot[tid >> 3] = ft;
     }
     __syncthreads();
-    prefix = (prefix << width) | static_cast<uint32_t>(sh.bcast[0]);
-    need = sh.bcast[1];
+    if (warp == 0) {
+      const int nd = sh.pick[pass][1];
+      const int cnt = sh.ftot[lane];
+      const int above = warp_suffix(cnt) - cnt;
+      if (above < nd && nd <= above + cnt) {
+        sh.pick[pass][2] = cbin * kFine + lane;
+        sh.pick[pass][3] = nd - above;
+      }
+    }
     __syncthreads();
+    prefix = (prefix << width) | static_cast<uint32_t>(sh.pick[pass][2]);
+    need = sh.pick[pass][3];
   }
   const uint32_t T = select_none ? 0xFFFFFFFFu : prefix;
   const int need_ties = select_none ? 0 : need;
@@ -250,39 +341,42 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 0) {
-    int g = sh.wgt[lane], e = sh.weq[lane], m = sh.wnm[lane];
+    int g = lane < kWarps ? sh.wgt[lane] : 0;
+    int e = lane < kWarps ? sh.weq[lane] : 0;
+    int m = lane < kWarps ? sh.wnm[lane] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
       e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
       m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
     }
-    if (lane == 0) {
-      sh.xch[0] = g;
-      sh.xch[1] = e;
-      sh.xch[2] = m;
-    }
+    if (lane == 0) sh.xch = make_int4(g, e, m, 0);
   }
-  cluster.sync();
+  cluster_sync_all();
   if (warp == 0) {
-    int eq_before = 0, keep_before = 0, M_b = 0, eq_run = 0;
-    for (int r = 0; r < kCluster; ++r) {
-      const int32_t *x = cluster.map_shared_rank(sh.xch, r);
-      const int ties_r = max(0, min(need_ties - eq_run, x[1]));
-      const int keep_r = x[0] + ties_r + x[2];
-      if (r < rank) {
-        eq_before += x[1];
-        keep_before += keep_r;
-      }
-      eq_run += x[1];
-      M_b += keep_r;
+    // lane r < kCluster holds rank r's counts; prefix over ranks in rank (= index) order
+    const int4 x = lane < kCluster ? ld_peer4(&sh.xch, lane) : make_int4(0, 0, 0, 0);
+    int eq_incl = x.y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, eq_incl, o);
+      if (lane >= o) eq_incl += t;
     }
-    if (rank == 0 && lane == 0) {
-      if (b == 0) p.cu_kept[0] = 0;
-      p.cu_kept[b + 1] = seq_offset + M_b;
+    const int eq_excl = eq_incl - x.y;
+    const int ties_r = max(0, min(need_ties - eq_excl, x.y));
+    const int keep_r = x.x + ties_r + x.z;
+    int keep_incl = keep_r;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, keep_incl, o);
+      if (lane >= o) keep_incl += t;
     }
+    const int eq_before = __shfl_sync(0xFFFFFFFFu, eq_excl, rank);
+    const int keep_before = __shfl_sync(0xFFFFFFFFu, keep_incl - keep_r, rank);
+    const int M_b = __shfl_sync(0xFFFFFFFFu, keep_incl, kCluster - 1);
+    if (lane == 0) sh.m_b = seq_offset + M_b;
     // per-warp tie base and output offset, in warp (= index) order
-    const int e = sh.weq[lane];
+    const int e = lane < kWarps ? sh.weq[lane] : 0;
     int e_incl = e;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -291,17 +385,25 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const int tie_base = eq_before + e_incl - e;
     const int ties_w = max(0, min(need_ties - tie_base, e));
-    const int keep_w = sh.wgt[lane] + sh.wnm[lane] + ties_w;
+    const int keep_w = lane < kWarps ? sh.wgt[lane] + sh.wnm[lane] + ties_w : 0;
     int k_incl = keep_w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(0xFFFFFFFFu, k_incl, o);
       if (lane >= o) k_incl += t;
     }
-    sh.wtie[lane] = tie_base;
-    sh.woff[lane] = seq_offset + keep_before + k_incl - keep_w;
+    if (lane < kWarps) {
+      sh.wtie[lane] = tie_base;
+      sh.woff[lane] = seq_offset + keep_before + k_incl - keep_w;
+    }
   }
   __syncthreads();
+  // this CTA is done reading its peers' shared memory (the loads have returned)
+  cluster_arrive_relaxed();
+  if (rank == 0 && tid == 0) {
+    if (b == 0) p.cu_kept[0] = 0;
+    p.cu_kept[b + 1] = sh.m_b;
+  }
 
   // ---- ordered write of this warp's kept rows ----
   int tie_run = sh.wtie[warp];
@@ -328,7 +430,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (overflow) tg::report(p.status, TG_DEV_CAPACITY);
   // keep this CTA's shared memory alive until every peer has finished reading it
-  cluster.sync();
+  cluster_wait();
 }
 
 }  // namespace
@@ -353,6 +455,8 @@ tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t 
   int keys = (T + kCluster - 1) / kCluster;
   keys = keys < 1 ? 1 : (keys > kMaxSmemKeys ? kMaxSmemKeys : keys);
   p.smem_keys = keys;
+  p.vec = (reinterpret_cast<uintptr_t>(s) % 16 == 0) &&
+          (mask == nullptr || reinterpret_cast<uintptr_t>(mask) % 4 == 0);
   const size_t smem = static_cast<size_t>(keys) * 4;
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
