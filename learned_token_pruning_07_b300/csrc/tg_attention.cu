@@ -221,26 +221,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
       bool ok = tg::mbar_wait(q_full, 0, vabort, p.wait_limit);
       int consumed = 0;
+      // descriptors of each operand buffer, built once; a K-step adds its byte offset / 16
+      // (buffers of one kind are contiguous, so buffer i is the first one's descriptor + i * tile / 16)
+      const uint64_t dq0 = tg::smem_desc(tg::smem_u32(sQ), 16, 1024, tg::kSwz128);
+      const uint64_t dk0 = tg::smem_desc(tg::smem_u32(sK), 16, 1024, tg::kSwz128);
+      const uint64_t dv0 = tg::smem_desc(tg::smem_u32(sV), 16384, 1024, tg::kSwz128);
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
       auto issue_s = [&](int t, int st) {
-        const uint32_t qa = tg::smem_u32(sQ + t * C::kTileBytes);
-        const uint32_t kb = tg::smem_u32(sK + st * C::kTileBytes);
+        const uint64_t qd = dq0 + t * kTile16, kd = dk0 + st * kTile16;
+        const uint32_t dst = tmem + colS[t];
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          const uint64_t ad = tg::smem_desc(qa + off, 16, 1024, tg::kSwz128);
-          const uint64_t bd = tg::smem_desc(kb + off, 16, 1024, tg::kSwz128);
-          tg::mma_bf16_ss(tmem + colS[t], ad, bd, idesc_s, k != 0);
+          const uint32_t off16 = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+          tg::mma_bf16_ss(dst, qd + off16, kd + off16, idesc_s, k != 0);
         }
         tg::mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int st, bool first) {
-        const uint32_t vb = tg::smem_u32(sV + st * C::kTileBytes);
+        const uint64_t vd = dv0 + st * kTile16;
+        const uint32_t dst = tmem + colO[t], src = tmem + colS[t];
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
           // keys 16k..16k+15: 16 rows of 128 B in every d-half; d-halves 16 KB apart
-          const uint64_t bd = tg::smem_desc(vb + k * 2048, 16384, 1024, tg::kSwz128);
-          tg::mma_bf16_ts(tmem + colO[t], tmem + colS[t] + k * 8, bd, idesc_o,
-                          !(first && k == 0));
+          tg::mma_bf16_ts(dst, src + k * 8, vd + ((k * 2048) >> 4), idesc_o, !(first && k == 0));
         }
       };
       if (ok) {
@@ -345,55 +348,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xFFFFFFFFu, w);  // tcgen05.ld below is warp-collective
         if (!ok) break;
         tg::tc_fence_after();
-        uint32_t sr[128];
-        {
-          uint32_t (&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-          uint32_t (&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          uint32_t (&a2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-          uint32_t (&a3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-          tg::tmem_ld_32x32b_x32(lane_addr + colS + 0, a0);
-          tg::tmem_ld_32x32b_x32(lane_addr + colS + 32, a1);
-          tg::tmem_ld_32x32b_x32(lane_addr + colS + 64, a2);
-          tg::tmem_ld_32x32b_x32(lane_addr + colS + 96, a3);
-          tg::tmem_ld_wait();
-        }
-        // logits in log2 units: x = s * scale + bias (pairs)
-        uint64_t x2[64];
+        // S row (128 fp32) -> logits in log2 units, in place: x = s * scale + bias
+        uint32_t x[128];
+        tg::tmem_ld_32x32b_x32(lane_addr + colS + 0, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tg::tmem_ld_32x32b_x32(lane_addr + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        tg::tmem_ld_32x32b_x32(lane_addr + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&x[64]));
+        tg::tmem_ld_32x32b_x32(lane_addr + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&x[96]));
+        tg::tmem_ld_wait();
         if (use_bias) {
           const float4 *bias4 = reinterpret_cast<const float4 *>(sBias + st * 256 + t * 128);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float4 bv = bias4[c];
-            x2[2 * c] = f2_fma(f2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), scale2,
-                               f2(bv.x, bv.y));
-            x2[2 * c + 1] = f2_fma(f2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])),
-                                   scale2, f2(bv.z, bv.w));
+            float a0, a1, a2, a3;
+            f2_split(f2_fma(f2(__uint_as_float(x[4 * c]), __uint_as_float(x[4 * c + 1])), scale2, f2(bv.x, bv.y)), a0, a1);
+            f2_split(f2_fma(f2(__uint_as_float(x[4 * c + 2]), __uint_as_float(x[4 * c + 3])), scale2, f2(bv.z, bv.w)), a2, a3);
+            x[4 * c] = __float_as_uint(a0);
+            x[4 * c + 1] = __float_as_uint(a1);
+            x[4 * c + 2] = __float_as_uint(a2);
+            x[4 * c + 3] = __float_as_uint(a3);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            x2[c] = f2_mul(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2);
+          for (int c = 0; c < 64; ++c) {
+            float a0, a1;
+            f2_split(f2_mul(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), scale2), a0, a1);
+            x[2 * c] = __float_as_uint(a0);
+            x[2 * c + 1] = __float_as_uint(a1);
+          }
         }
-        float tile_max = -INFINITY;
         if (j == tq) {
           // diagonal tile: key c is visible to row r only when c <= r
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            float a, bb;
-            f2_split(x2[c], a, bb);
-            a = (2 * c > r) ? -INFINITY : a;
-            bb = (2 * c + 1 > r) ? -INFINITY : bb;
-            x2[c] = f2(a, bb);
-            tile_max = fmax3(tile_max, a, bb);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            float a, bb;
-            f2_split(x2[c], a, bb);
-            tile_max = fmax3(tile_max, a, bb);
-          }
+          for (int c = 0; c < 128; ++c)
+            if (c > r) x[c] = __float_as_uint(-INFINITY);
         }
+        // row max over 8 independent chains, then combined
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(__uint_as_float(x[i]), __uint_as_float(x[8 + i]), __uint_as_float(x[16 + i]));
+#pragma unroll
+        for (int c = 24; c < 128; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
+        }
+        const float tile_max = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         // lazy max update; rescale O and l only when the max moved by more than the threshold
         float alpha = 1.0f;
         bool rescale = false;
@@ -406,18 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
         const uint64_t negm2 = f2(-m_use, -m_use);
-        uint64_t sum2 = f2(0.0f, 0.0f);
-        uint32_t pk[64];
+        // p = 2^(x - m), packed to bf16 pairs in place (x[c] is dead once pair c/2 is done);
+        // the row sum runs on four independent pair accumulators
+        uint64_t sum2[4] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f), f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float a, bb;
-          f2_split(f2_add(x2[c], negm2), a, bb);
+          f2_split(f2_add(f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), negm2), a, bb);
           const float pa = ex2(a), pb = ex2(bb);
-          sum2 = f2_add(sum2, f2(pa, pb));
-          pk[c] = tg::pack_bf16x2(pa, pb);
+          sum2[c & 3] = f2_add(sum2[c & 3], f2(pa, pb));
+          x[c] = tg::pack_bf16x2(pa, pb);
         }
-        float s_lo, s_hi;
-        f2_split(sum2, s_lo, s_hi);
+        float s_lo, s_hi, t_lo, t_hi;
+        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s_lo, s_hi);
+        (void)t_lo;
+        (void)t_hi;
         l = l * alpha + (s_lo + s_hi);
         if (__any_sync(0xFFFFFFFFu, rescale)) {
           // O_t *= alpha for this row (the PV of step j-1 into O_t has completed: S_t(j) was
@@ -432,12 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P (bf16 pairs) over the first 64 columns of S_t
-        {
-          uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-          uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-          tg::tmem_st_32x32b_x32(lane_addr + colS + 0, p0);
-          tg::tmem_st_32x32b_x32(lane_addr + colS + 32, p1);
-        }
+        tg::tmem_st_32x32b_x32(lane_addr + colS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&x[0]));
+        tg::tmem_st_32x32b_x32(lane_addr + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&x[32]));
         tg::tmem_st_wait();
         tg::tc_fence_before();
         tg::mbar_arrive(&p_full[t]);

@@ -43,13 +43,18 @@ __device__ __forceinline__ void st_cs_v4(uint4 *p, uint4 v) {
 }
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
-  int M = min(p.cu_kept[p.B], p.capacity);
-  if (M < 0) M = 0;
   const int lane = threadIdx.x & 31;
   const int nvec = p.d >> 3;  // 16-byte vectors per row
   const int stride = gridDim.x * kGatherWarps;
-  for (int m = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); m < M; m += stride) {
-    const int j = p.kept_idx[m];
+  const int m0 = blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+  // the first row's index is fetched together with the kept count (both sit in L2 from the
+  // selection); an index at m >= M is read from inside the buffer but never used
+  int j_next = m0 < p.capacity ? p.kept_idx[m0] : -1;
+  int M = min(p.cu_kept[p.B], p.capacity);
+  if (M < 0) M = 0;
+  for (int m = m0; m < M; m += stride) {
+    const int j = j_next;
+    if (m + stride < M) j_next = p.kept_idx[m + stride];
     if (j < 0 || j >= p.T) {
       if (lane == 0) tg::report(p.status, TG_DEV_BAD_INDEX);
       continue;

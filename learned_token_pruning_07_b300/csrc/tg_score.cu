@@ -1,26 +1,38 @@
 // tg_score.cu — gate scoring (TokenGate deep dive, section 3.1, Eq. (3): b~_j = MLP(a~_j)).
 //
-// One CTA owns a 128-row tile of hidden states and the full d_g-wide hidden layer of the
-// score MLP. The d-reduction u = h W1^T runs on the tensor cores (tcgen05.mma kind::f16,
-// bf16 operands staged by TMA into 64-byte-swizzled shared memory, fp32 accumulator in
-// tensor memory: 128 lanes x d_g columns). The epilogue reads each row's accumulator
-// out of tensor memory and finishes the MLP in fp32 registers:
-//   s = w2 . SiLU(u + b1) + b2,  g = sigmoid(s)  (g = 1 on non-prunable rows).
-// Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warp 2 owns the tensor-memory
-// allocation, all four warps run the epilogue (warp w reads TMEM lanes 32w..32w+31).
+//   u = W1 h_j (+ b1),  s_j = w2 . SiLU(u) (+ b2),  g_j = sigmoid(s_j)  (g = 1 on non-prunable rows)
+//
+// Persistent kernel: one CTA per SM; CTAs run in clusters of two that walk pairs of
+// neighbouring 128-row tiles of h in lockstep. Each CTA of a pair loads its own h tile and
+// HALF of every W1 stage, multicasting that half into both CTAs, so each SM pulls half the
+// W1 bytes through L2 (W1 is re-read for every tile: without sharing it is 4x the h bytes). The d_g-wide hidden layer of a tile is computed as n_items column
+// slices of at most 256 (two slices of 256 at d_g = 512). Each slice is one work item: a
+// d-reduction u_slice = h_tile W1_slice^T on the tensor cores (tcgen05.mma kind::f16, bf16
+// operands staged by TMA into 128-byte-swizzled shared memory, fp32 accumulator in one of
+// two 256-column tensor-memory buffers). The epilogue of item i (SiLU, the w2 dot, and at a
+// tile's last slice the sigmoid) runs while the tensor cores already work on item i+1 in the
+// other buffer. A row's partial w2 dots of its slices are summed in registers by the same
+// thread, in slice order, so s is deterministic and no scratch memory is needed.
+//
+// Warp roles: warp 0 lane 0 issues TMA; warp 1 owns tensor memory and lane 0 issues MMAs;
+// warps 2-5 run the epilogue (warp w reads tensor-memory lanes 32*(w%4) .. +31, one row per
+// thread). Every wait is bounded (see tg_set_wait_limit_ns); a wait that gives up sets
+// TG_DEV_TIMEOUT, drains the copies and MMAs in flight, frees tensor memory and returns.
 #include "tg_common.cuh"
 
 namespace {
 
 constexpr int kBM = 128;      // rows per tile = tensor-memory lanes
-constexpr int kBK = 32;       // d-elements per pipeline stage (one 64-byte swizzled row)
-constexpr int kStages = 5;
-constexpr int kThreads = 128;
+constexpr int kBK = 64;       // d-elements per pipeline stage (one 128-byte swizzled row)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
 constexpr int kMaxDg = 512;
+constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
+constexpr uint32_t kTmemCols = 2 * kMaxItemN;
+constexpr int kPair = 2;  // CTAs of a cluster: neighbouring row tiles that share each W1 stage
 
 struct ScoreParams {
-  int32_t T, d, d_g, n_inst, n_split;
-  uint32_t tmem_cols;
+  int32_t T, d, d_g, n_items, item_n, n_tiles, KT;
   const float *b1;
   const uint16_t *w2;
   float b2;
@@ -35,10 +47,10 @@ struct SmemLayout {
   uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_bar, total;
 };
 
-__host__ __device__ inline SmemLayout score_smem_layout(int d_g) {
+__host__ __device__ inline SmemLayout score_smem_layout(int item_n) {
   SmemLayout L;
-  L.a_bytes = kBM * kBK * 2;
-  L.b_bytes = static_cast<uint32_t>(d_g) * kBK * 2;
+  L.a_bytes = kBM * kBK * 2;                               // 16 KB
+  L.b_bytes = static_cast<uint32_t>(item_n) * kBK * 2;     // <= 32 KB, a multiple of 1 KB
   L.off_b = kStages * L.a_bytes;
   L.off_w2 = L.off_b + kStages * L.b_bytes;
   L.off_b1 = L.off_w2 + kMaxDg * 4;
@@ -47,21 +59,49 @@ __host__ __device__ inline SmemLayout score_smem_layout(int d_g) {
   return L;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// TMA tile load of W1 rows that lands at the same shared-memory offset in every CTA of the
+// pair and signals the barrier at the same offset in each (cluster multicast).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(tg::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tg::smem_u32(bar)), "r"(x), "r"(y),
+      "h"(static_cast<uint16_t>((1u << kPair) - 1u))
+      : "memory");
+}
+
+// Arrive once on the barrier at this offset in both CTAs of the pair when every MMA issued
+// so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(tg::smem_u32(bar)),
+      "h"(static_cast<uint16_t>((1u << kPair) - 1u))
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
-                      const __grid_constant__ CUtensorMap tm_w, ScoreParams p) {
+                      const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = score_smem_layout(p.d_g);
+  const SmemLayout L = score_smem_layout(p.item_n);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
   float *s_w2 = reinterpret_cast<float *>(smem + L.off_w2);
   float *s_b1 = reinterpret_cast<float *>(smem + L.off_b1);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
   uint64_t *empty = full + kStages;
-  uint64_t *accum = empty + kStages;
-  uint64_t *drain = accum + 1;
+  uint64_t *acc_full = empty + kStages;  // [2] MMA -> epilogue
+  uint64_t *acc_empty = acc_full + 2;    // [2] epilogue -> MMA
+  uint64_t *drain = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
@@ -73,9 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       tg::mbar_init(&full[i], 1);
-      tg::mbar_init(&empty[i], 1);
+      tg::mbar_init(&empty[i], kPair);  // one MMA commit from each CTA of the pair
     }
-    tg::mbar_init(accum, 1);
+    for (int i = 0; i < 2; ++i) {
+      tg::mbar_init(&acc_full[i], 1);
+      tg::mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
+    }
     tg::mbar_init(drain, 1);
     *abort_flag = 0;
     *n_issued = 0;
@@ -84,8 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tg::prefetch_tensormap(&tm_h);
     tg::prefetch_tensormap(&tm_w);
   }
-  if (warp == 2) {
-    tg::tmem_alloc(tmem_slot, p.tmem_cols);
+  if (warp == 1) {
+    tg::tmem_alloc(tmem_slot, kTmemCols);
     tg::tmem_relinquish();
   }
   for (int i = threadIdx.x; i < p.d_g; i += kThreads) {
@@ -93,104 +136,134 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
   tg::tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any multicast arrives
   tg::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int row0 = blockIdx.x * kBM;
-  const int KT = p.d / kBK;
   volatile int32_t *vabort = abort_flag;
+  const uint32_t stage_bytes = L.a_bytes + L.b_bytes;
+  // the pair (cluster) walks tile pairs in lockstep; this CTA owns tile 2 * pair + rank
+  uint32_t rank;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int pair0 = blockIdx.x / kPair;
+  const int pair_stride = gridDim.x / kPair;
+  const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
+  const int half_n = p.item_n / kPair;  // W1 rows of a stage this CTA loads for both
 
   if (warp == 0) {
     if (lane == 0) {
-      // TMA producer: fill stage st with the h tile [128 x 32] and W1 slice [d_g x 32].
-      int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int st = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!tg::mbar_wait(&empty[st], ph ^ 1u, vabort, p.wait_limit)) {
-          *vabort = 1;
-          break;
+      // ---- TMA producer: stage = h tile [128 x 64] + W1 slice [item_n x 64] ----
+      int kc = 0;
+      bool ok = true;
+      for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
+        // a tile past the end (odd tile count) re-reads the last tile; its rows are not stored
+        const int tile = min(pr * kPair + static_cast<int>(rank), p.n_tiles - 1);
+        for (int item = 0; item < p.n_items && ok; ++item) {
+          for (int kt = 0; kt < p.KT; ++kt, ++kc) {
+            const int st = kc % kStages;
+            if (!tg::mbar_wait(&empty[st], ((kc / kStages) & 1) ^ 1u, vabort, p.wait_limit)) {
+              *vabort = 1;
+              ok = false;
+              break;
+            }
+            // this stage receives: own h tile + both halves of the W1 slice (one from each CTA)
+            tg::mbar_arrive_expect_tx(&full[st], stage_bytes);
+            tg::tma_load_2d(sA + st * L.a_bytes, &tm_h, &full[st], kt * kBK, tile * kBM);
+            tma_load_2d_pair(sB + st * L.b_bytes + rank * half_n * (kBK * 2), &tm_w, &full[st],
+                             kt * kBK, item * p.item_n + static_cast<int>(rank) * half_n);
+            *n_issued = kc + 1;
+          }
         }
-        tg::mbar_arrive_expect_tx(&full[st], L.a_bytes + L.b_bytes);
-        tg::tma_load_2d(sA + st * L.a_bytes, &tm_h, &full[st], kt * kBK, row0);
-        for (int j = 0; j < p.n_split; ++j)
-          tg::tma_load_2d(sB + st * L.b_bytes + j * p.n_inst * (kBK * 2), &tm_w, &full[st],
-                          kt * kBK, j * p.n_inst);
-        issued = kt + 1;
       }
-      *n_issued = issued;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issuer: u[128 x d_g] += A[128 x 16] * B[d_g x 16]^T, two K-steps per stage.
-      const uint32_t idesc = tg::idesc_bf16_f32(kBM, p.n_inst);
-      int consumed = 0;
+      // ---- MMA issuer: u_slice[128 x item_n] += A[128 x 16] * B[item_n x 16]^T ----
+      const uint32_t idesc = tg::idesc_bf16_f32(kBM, p.item_n);
+      int kc = 0, it = 0;
       bool ok = true;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int st = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!tg::mbar_wait(&full[st], ph, vabort, p.wait_limit)) {
-          *vabort = 1;
-          ok = false;
-          break;
-        }
-        tg::tc_fence_after();
-        const uint32_t a_base = tg::smem_u32(sA + st * L.a_bytes);
-        const uint32_t b_base = tg::smem_u32(sB + st * L.b_bytes);
-#pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          const uint64_t a_desc = tg::smem_desc(a_base + ks * 32, 16, 8 * kBK * 2, tg::kSwz64);
-          for (int j = 0; j < p.n_split; ++j) {
-            const uint64_t b_desc = tg::smem_desc(b_base + j * p.n_inst * (kBK * 2) + ks * 32,
-                                                  16, 8 * kBK * 2, tg::kSwz64);
-            tg::mma_bf16_ss(tmem + j * p.n_inst, a_desc, b_desc, idesc, (kt | ks) != 0);
+      for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
+        for (int item = 0; item < p.n_items && ok; ++item, ++it) {
+          const int buf = it & 1;
+          if (!tg::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1u, vabort, p.wait_limit)) {
+            ok = false;
+            break;
           }
+          tg::tc_fence_after();
+          const uint32_t d_tmem = tmem + buf * kMaxItemN;
+          for (int kt = 0; kt < p.KT; ++kt, ++kc) {
+            const int st = kc % kStages;
+            if (!tg::mbar_wait(&full[st], (kc / kStages) & 1, vabort, p.wait_limit)) {
+              ok = false;
+              break;
+            }
+            tg::tc_fence_after();
+            const uint32_t a_base = tg::smem_u32(sA + st * L.a_bytes);
+            const uint32_t b_base = tg::smem_u32(sB + st * L.b_bytes);
+#pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+              const uint64_t a_desc = tg::smem_desc(a_base + ks * 32, 16, 1024, tg::kSwz128);
+              const uint64_t b_desc = tg::smem_desc(b_base + ks * 32, 16, 1024, tg::kSwz128);
+              tg::mma_bf16_ss(d_tmem, a_desc, b_desc, idesc, (kt | ks) != 0);
+            }
+            mma_commit_pair(&empty[st]);  // the stage is free once both CTAs have read it
+            *n_consumed = kc + 1;
+          }
+          if (ok) tg::mma_commit(&acc_full[buf]);
         }
-        tg::mma_commit(&empty[st]);
-        consumed = kt + 1;
       }
-      *n_consumed = consumed;
-      if (ok) {
-        tg::mma_commit(accum);
-      } else {
+      if (!ok) {
+        *vabort = 1;
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
         tg::mma_commit(drain);
         volatile int32_t never = 0;
         tg::mbar_wait(drain, 0, &never, p.wait_limit);
       }
     }
-  }
-  __syncwarp();
-
-  // Epilogue: every thread owns one row of the tile.
-  // tcgen05.ld is warp-collective: the whole warp takes the same branch.
-  const bool acc_ok = __all_sync(0xffffffffu, tg::mbar_wait(accum, 0, vabort, p.wait_limit));
-  tg::tc_fence_after();
-  if (acc_ok) {
-    const int row = row0 + warp * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float acc = 0.0f;
-    uint32_t r[32];
-    for (int c0 = 0; c0 < p.d_g; c0 += 32) {
-      tg::tmem_ld_32x32b_x32(lane_base + c0, r);
-      tg::tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float u = __uint_as_float(r[i]) + s_b1[c0 + i];
-        const float silu = __fdividef(u, 1.0f + __expf(-u));
-        acc = fmaf(s_w2[c0 + i], silu, acc);
-      }
-    }
-    if (row < p.T) {
-      const float s = acc + p.b2;
-      p.s_out[row] = s;
-      if (p.g_out) {
-        const bool keep_always = p.mask && p.mask[row];
-        p.g_out[row] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
-      }
-    }
   } else {
-    *vabort = 1;
+    // ---- epilogue: one row per thread; SiLU . w2 over each slice, sigmoid at the end ----
+    const int quarter = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int it = 0;
+    bool ok = true;
+    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
+      const int tile = pr * kPair + static_cast<int>(rank);
+      float acc = 0.0f;
+      for (int item = 0; item < p.n_items; ++item, ++it) {
+        const int buf = it & 1;
+        // tcgen05.ld is warp-collective: the whole warp takes the same branch
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_full[buf], (it >> 1) & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        tg::tc_fence_after();
+        const uint32_t col0 = static_cast<uint32_t>(buf * kMaxItemN);
+        const int hid0 = item * p.item_n;
+        for (int c0 = 0; c0 < p.item_n; c0 += 32) {
+          uint32_t v[32];
+          tg::tmem_ld_32x32b_x32(lane_base + col0 + c0, v);
+          tg::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float u = __uint_as_float(v[i]) + s_b1[hid0 + c0 + i];
+            const float silu = __fdividef(u, 1.0f + __expf(-u));
+            acc = fmaf(s_w2[hid0 + c0 + i], silu, acc);
+          }
+        }
+        tg::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tg::mbar_arrive(&acc_empty[buf]);
+      }
+      if (!ok) break;
+      const int row = tile * kBM + r;
+      if (row < p.T) {
+        const float s = acc + p.b2;
+        p.s_out[row] = s;
+        if (p.g_out) {
+          const bool keep_always = p.mask && p.mask[row];
+          p.g_out[row] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
+        }
+      }
+    }
+    if (!ok) *vabort = 1;
   }
 
   tg::tc_fence_before();
@@ -205,10 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tg::tc_fence_after();
-    tg::tmem_dealloc(tmem, p.tmem_cols);
+    tg::tmem_dealloc(tmem, kTmemCols);
   }
+  // neither CTA leaves while its peer may still signal its barriers or write its stages
+  cluster_sync_all();
 }
 
 }  // namespace
@@ -224,11 +299,10 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   p.T = T;
   p.d = d;
   p.d_g = d_g;
-  p.n_split = d_g > 256 ? 2 : 1;
-  p.n_inst = d_g / p.n_split;
-  uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(d_g)) cols <<= 1;
-  p.tmem_cols = cols;
+  p.n_items = d_g > kMaxItemN ? 2 : 1;
+  p.item_n = d_g / p.n_items;  // d_g % 32 == 0, so a multiple of 16, at most 256
+  p.n_tiles = (T + kBM - 1) / kBM;
+  p.KT = (d + kBK - 1) / kBK;  // a ragged last stage reads zeros past d from both operands
   p.b1 = b1;
   p.w2 = w2;
   p.b2 = b2;
@@ -243,22 +317,24 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
     const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(T)};
     const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
     const uint32_t box[2] = {kBK, kBM};
-    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(d_g)};
     const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.n_inst)};
-    if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.item_n / kPair)};
+    if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
-  const SmemLayout L = score_smem_layout(d_g);
+  const SmemLayout L = score_smem_layout(p.item_n);
   cudaError_t e = cudaFuncSetAttribute(gate_score_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
-  const int grid = (T + kBM - 1) / kBM;
-  gate_score_kernel<<<grid, kThreads, L.total, stream>>>(tm_h, tm_w, p);
+  const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
+  int pairs = num_sms() / kPair;
+  if (pairs > n_pairs) pairs = n_pairs;
+  gate_score_kernel<<<pairs * kPair, kThreads, L.total, stream>>>(tm_h, tm_w, p);
   return record_cuda(cudaGetLastError());
 }
 
