@@ -36,6 +36,7 @@ SIGNATURES = {
     "tg_apply_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "tg_read_device_status": (_I, [_P, _P, _P]),
     "tg_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "tg_set_test_withhold": (_I, [_I]),
 }
 
 
@@ -169,3 +170,11 @@ def read_device_status(status, stream=None) -> int:
 
 def set_wait_limit_ns(ns: int):
     _check("tg_set_wait_limit_ns", load().tg_set_wait_limit_ns(int(ns)))
+
+
+TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION = 1, 2
+
+
+def set_test_withhold(mask: int):
+    """Test hook: make the named kernels issue no loads so their bounded waits run out."""
+    _check("tg_set_test_withhold", load().tg_set_test_withhold(int(mask)))

@@ -52,7 +52,8 @@ struct AttnParams {
   int32_t B, M_cap, max_seqlen, H_q, H_kv, group, heads_per_cta, pairs, n_qt_max;
   uint16_t *O;
   int32_t *status;
-  uint64_t wait_limit;
+  uint64_t wait_limit, drain_limit;
+  int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
   float scale_log2[kMaxHeads];  // tau_h * log2(e) / sqrt(d_h)
   float beta[kMaxHeads];
 };
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
   int32_t *n_consumed = abort_flag + 2;
+  int32_t *q_issued = abort_flag + 3;
   volatile int32_t *vabort = abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     *n_issued = 0;
     *n_consumed = 0;
+    *q_issued = 0;
     tg::fence_mbar_init();
     tg::prefetch_tensormap(&tm_q);
     tg::prefetch_tensormap(&tm_k);
@@ -186,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.withhold) {
       // ---------------- TMA producer ----------------
+      *q_issued = 1;
       tg::mbar_arrive_expect_tx(q_full, n_tiles * C::kTileBytes);
       for (int t = 0; t < n_tiles; ++t)
         for (int hf = 0; hf < C::kHalves; ++hf)
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *vabort = 1;
         tg::mma_commit(drain);
         volatile int32_t never = 0;
-        tg::mbar_wait(drain, 0, &never, p.wait_limit);
+        tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
     }
   } else if (warp == 2) {
@@ -475,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::report(p.status, TG_DEV_TIMEOUT);
       volatile int32_t never = 0;
       for (int i = *n_consumed; i < *n_issued; ++i)
-        tg::mbar_wait(&kv_full[i % C::kStages], (i / C::kStages) & 1, &never, p.wait_limit);
-      tg::mbar_wait(q_full, 0, &never, p.wait_limit);
+        tg::mbar_wait(&kv_full[i % C::kStages], (i / C::kStages) & 1, &never, p.drain_limit);
+      if (*q_issued) tg::mbar_wait(q_full, 0, &never, p.drain_limit);
     }
     __syncthreads();
   }
@@ -547,6 +551,8 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
   p.O = O;
   p.status = status;
   p.wait_limit = wait_limit_ns();
+  p.drain_limit = drain_limit_ns();
+  p.withhold = (withhold_mask() & TG_WITHHOLD_ATTENTION) != 0;
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale_log2[h] = h < H_q ? tau[h] * log2e / std::sqrt(static_cast<float>(d_h)) : 0.0f;

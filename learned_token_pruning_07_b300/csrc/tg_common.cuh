@@ -286,6 +286,8 @@ bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64
                       const uint64_t *strides_bytes, const uint32_t *box,
                       CUtensorMapSwizzle swizzle);
 uint64_t wait_limit_ns();
+uint64_t drain_limit_ns();
+int32_t withhold_mask();
 int num_sms();
 tg_status record_cuda(cudaError_t e);
 }  // namespace tg_host

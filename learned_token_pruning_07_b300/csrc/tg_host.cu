@@ -11,6 +11,7 @@
 namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int32_t> g_withhold{0};
 thread_local int32_t g_last_cuda_error = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -56,6 +57,15 @@ bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+// Waits for a kernel's own copies and MMAs in flight, after a pipeline wait gave up: never
+// shorter than 0.2 s, so a small test limit cannot let a CTA exit while a copy still lands.
+uint64_t drain_limit_ns() {
+  const uint64_t w = wait_limit_ns();
+  return w > 200000000ull ? w : 200000000ull;
+}
+
+int32_t withhold_mask() { return g_withhold.load(std::memory_order_relaxed); }
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -92,6 +102,12 @@ int32_t tg_last_cuda_error(void) { return g_last_cuda_error; }
 
 tg_status tg_set_wait_limit_ns(uint64_t limit_ns) {
   g_wait_limit_ns.store(limit_ns == 0 ? 2000000000ull : limit_ns, std::memory_order_relaxed);
+  return TG_OK;
+}
+
+tg_status tg_set_test_withhold(int32_t mask) {
+  if (mask & ~(TG_WITHHOLD_GATE_SCORE | TG_WITHHOLD_ATTENTION)) return TG_ERR_INVALID_ARG;
+  g_withhold.store(mask, std::memory_order_relaxed);
   return TG_OK;
 }
 

@@ -40,7 +40,8 @@ struct ScoreParams {
   float *s_out;
   float *g_out;
   int32_t *status;
-  uint64_t wait_limit;
+  uint64_t wait_limit, drain_limit;
+  int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
 };
 
 struct SmemLayout {
@@ -153,7 +154,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---- TMA producer: stage = h tile [128 x 64] + W1 slice [item_n x 64] ----
       int kc = 0;
-      bool ok = true;
+      bool ok = !p.withhold;
       for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
         // a tile past the end (odd tile count) re-reads the last tile; its rows are not stored
         const int tile = min(pr * kPair + static_cast<int>(rank), p.n_tiles - 1);
@@ -216,7 +217,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
         tg::mma_commit(drain);
         volatile int32_t never = 0;
-        tg::mbar_wait(drain, 0, &never, p.wait_limit);
+        tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
     }
   } else {
@@ -274,7 +275,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
       // wait (bounded) for TMA copies that were issued but never consumed
       volatile int32_t never = 0;
       for (int i = *n_consumed; i < *n_issued; ++i)
-        tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.wait_limit);
+        tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.drain_limit);
     }
     __syncthreads();
   }
@@ -311,6 +312,8 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   p.g_out = g_out;
   p.status = status;
   p.wait_limit = wait_limit_ns();
+  p.drain_limit = drain_limit_ns();
+  p.withhold = (withhold_mask() & TG_WITHHOLD_GATE_SCORE) != 0;
 
   CUtensorMap tm_h, tm_w;
   {

@@ -89,3 +89,9 @@ def test_rope_rejects_bad_arguments(lib):
 def test_wait_limit_setter(lib):
     assert lib.tg_set_wait_limit_ns(1000) == binding.TG_OK
     assert lib.tg_set_wait_limit_ns(0) == binding.TG_OK
+
+
+def test_test_withhold_hook_validates_its_mask(lib):
+    assert lib.tg_set_test_withhold(binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION) == binding.TG_OK
+    assert lib.tg_set_test_withhold(4) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_set_test_withhold(0) == binding.TG_OK
