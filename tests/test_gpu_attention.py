@@ -108,3 +108,38 @@ def test_attention_ragged_batch_sampled_rows():
     cu = I.cu_seqlens_of(lens)
     rows = sampled_rows(cu, [], 600, seed=6)
     _assert_close(*_run(wl, lens, rows=rows))
+
+
+def test_attention_long_context_pruned_sampled_rows():
+    # 128K context pruned to K = 8192 document tokens plus 512 instruction tokens
+    wl = I.WORKLOADS["long_128k"]
+    M = 8192 + 512
+    cu = I.cu_seqlens_of([M])
+    rows = sampled_rows(cu, list(range(M - 512, M)), 700, seed=7)
+    _assert_close(*_run(wl, [M], rows=rows))
+
+
+@pytest.mark.slow
+def test_attention_long_context_full_causal_sampled_rows():
+    # the layers at or below the gate: plain causal GQA over all 131,584 tokens (no gate,
+    # tau = 1, beta = 0), the unpruned side of the long-context comparison
+    wl = I.with_changes(I.WORKLOADS["long_128k"], fixed_tau_beta=1.0)
+    M = wl.T_total
+    cu = I.cu_seqlens_of([M])
+    rows = sampled_rows(cu, [], 160, seed=8)
+    at = I.make_attention_inputs(wl, M)
+    beta = np.zeros(wl.H_q, np.float32)
+    O_d = torch.full((M, wl.H_q, wl.d_h), 0x7FC0, dtype=torch.int16, device="cuda")
+    st = status_word()
+    tg.gated_attention(dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(cu), at["tau"], beta, O_d,
+                       max_seqlen=M, g=None, status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    got = I.bf16_bits_to_f64(host(O_d[torch.from_numpy(rows).cuda()]))
+    del O_d
+    # fp64 query rows only where sampled (np.zeros pages are not touched elsewhere)
+    Q64 = np.zeros((M, wl.H_q, wl.d_h))
+    Q64[rows] = I.bf16_bits_to_f64(at["Q"][rows])
+    ref = O.gated_attention(Q64, I.bf16_bits_to_f64(at["K"]), I.bf16_bits_to_f64(at["V"]), None, cu,
+                            at["tau"].astype(np.float64), beta.astype(np.float64), rows=rows)
+    _assert_close(got, ref)
