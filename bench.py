@@ -405,6 +405,55 @@ def cpu_baseline(wl, K, frac, budget_s=20.0):
 # main
 # ---------------------------------------------------------------------------
 
+def long_context(torch, flush, steps):
+    """The 128K long-context workload: one pruned step (K = 8192) against full causal GQA
+    attention over all 131,584 tokens, the attention the layers at or below the gate run."""
+    from learned_token_pruning_07_b300 import inputs as I
+    wl = I.WORKLOADS["long_128k"]
+    path = GatedPrefill(wl, wl.K, torch)
+    g = GraphStep(path, torch)
+    warm(g, 3, torch, flush)
+    ps, pst = time_device_steps(g, max(3, min(steps, 10)), torch, flush)
+    wk = stage_work(wl, wl.K, path.kept_lens)
+    del g, path
+    torch.cuda.empty_cache()
+    # full causal attention: seeded synthetic Q/K/V made on the device (timing only)
+    M = wl.T_total
+    gen = torch.Generator(device="cuda").manual_seed(wl.seed)
+    Q = torch.randn((M, wl.H_q, wl.d_h), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    Kt = torch.randn((M, wl.H_kv, wl.d_h), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    V = torch.randn((M, wl.H_kv, wl.d_h), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    O = torch.empty_like(Q)
+    cu = torch.tensor([0, M], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tau, beta = np.ones(wl.H_q, np.float32), np.zeros(wl.H_q, np.float32)
+    from learned_token_pruning_07_b300 import binding as tg
+    call = lambda: tg.gated_attention(Q, Kt, V, cu, tau, beta, O, max_seqlen=M, g=None, status=st)
+    call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    assert tg.read_device_status(st) == 0, "device reported an error"
+    full_ms = float(np.median(times))
+    full_flops = 4.0 * wl.d_h * wl.H_q * M * (M + 1) / 2
+    del Q, Kt, V, O
+    torch.cuda.empty_cache()
+    pruned_attn_ms = float(pst[:, 3].mean())
+    return {"workload": workload_label(wl, wl.K) + "; full causal attention over all tokens",
+            "pruned_step_ms": float(ps.mean()), "pruned_tokens_per_s": wl.T_total / (float(ps.mean()) / 1000.0),
+            "pruned_stage_us": [float(x) * 1000.0 for x in pst.mean(axis=0)],
+            "pruned_attention_tflops": wk["gated_attention"]["flops"] / (pruned_attn_ms * 1e-3) / 1e12,
+            "full_attention_ms": full_ms, "full_attention_tflops": full_flops / (full_ms * 1e-3) / 1e12,
+            "attention_time_ratio_full_over_pruned": full_ms / pruned_attn_ms}
+
+
 def workload_label(wl, K):
     docs = wl.doc_lens if wl.B > 1 else wl.doc_lens[0]
     ins = wl.instr_lens if wl.B > 1 else wl.instr_lens[0]
@@ -539,6 +588,8 @@ def run_gpu(args, rank, world, local):
                 del g2, p2
                 torch.cuda.empty_cache()
 
+    longctx = long_context(torch, flush, args.steps) if (args.long_context and rank == 0) else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(base, K, args.oracle_frac)
@@ -567,6 +618,8 @@ def run_gpu(args, rank, world, local):
         }
         if sweep:
             line["sweep"] = sweep
+        if longctx:
+            line["long_context"] = longctx
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -583,6 +636,8 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=None)
     ap.add_argument("--sweep", action=argparse.BooleanOptionalAction, default=True)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--long-context", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the 128K workload: pruned step vs full causal attention")
     ap.add_argument("--oracle-frac", type=int, default=8)
     args = ap.parse_args(argv)
     if args.warmup < 3:
