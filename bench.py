@@ -228,25 +228,22 @@ class GatedPrefill:
         self.O_host = torch.empty(self.O.shape, dtype=torch.int16).pin_memory()
         self.cu_kept_host = torch.empty(B + 1, dtype=torch.int32).pin_memory()
 
-    def step(self, ev=None):
-        """K1..K4 on device-resident inputs; ev = 5 events recorded around the kernels."""
+    def step(self, ev=(None,) * 5):
+        """K1..K4 on device-resident inputs; ev = 5 events (or None) recorded around the kernels.
+        An event between two kernels also separates them (no launch overlap across it)."""
         tg, d = self.tg, self.d
-        if ev:
-            ev[0].record()
+        rec = lambda e: e.record() if e is not None else None
+        rec(ev[0])
         tg.gate_score(d["h"], self.W1, self.w2, self.s, self.g, instr_mask=d["mask"], status=self.status)
-        if ev:
-            ev[1].record()
+        rec(ev[1])
         tg.topk_select(self.s, d["cu"], self.K, self.kept, self.cu_kept, instr_mask=d["mask"], status=self.status)
-        if ev:
-            ev[2].record()
+        rec(ev[2])
         tg.gather_kept(d["h"], d["cu"], self.kept, self.cu_kept, self.h_kept, pos=d["pos"], g=self.g,
                        pos_kept=self.pos_kept, g_kept=self.g_kept, status=self.status)
-        if ev:
-            ev[3].record()
+        rec(ev[3])
         tg.gated_attention(d["Q"], d["K"], d["V"], self.cu_kept, self.tau, self.beta, self.O,
                            max_seqlen=self.max_seqlen, g=self.g_kept, status=self.status)
-        if ev:
-            ev[4].record()
+        rec(ev[4])
 
     def step_e2e(self):
         """The public fused call with host buffers: H2D of the step's activations, the path,
@@ -270,26 +267,40 @@ class GatedPrefill:
 
 
 class GraphStep:
-    """The four-kernel step captured once in a CUDA graph, with timing-event record nodes
-    between the kernels, so host launch overhead never shows up on the device timeline."""
+    """The four-kernel step captured once in CUDA graphs, so host launch overhead never shows
+    up on the device timeline. Two graphs: `whole` records events only around the step, so
+    each kernel's launch may overlap the previous kernel's tail (programmatic dependent
+    launch) -- this one gives the step time; `staged` records an event between every two
+    kernels and gives the per-kernel breakdown."""
 
     def __init__(self, path, torch):
         self.torch = torch
         self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        self.ew = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
         path.step()                      # first launch sets kernel attributes outside capture
         torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
+        self.staged = self._capture(path, self.ev)
+        self.whole = self._capture(path, [self.ew[0], None, None, None, self.ew[1]])
+        self.graph = self.whole
+
+    def _capture(self, path, ev):
+        torch = self.torch
+        graph = torch.cuda.CUDAGraph()
         stream = torch.cuda.Stream()
         stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
-            self.graph.capture_begin(capture_error_mode="relaxed")
-            path.step(self.ev)
-            self.graph.capture_end()
+            graph.capture_begin(capture_error_mode="relaxed")
+            path.step(ev)
+            graph.capture_end()
         torch.cuda.current_stream().wait_stream(stream)
         torch.cuda.synchronize()
+        return graph
 
-    def replay(self):
-        self.graph.replay()
+    def replay(self, staged=False):
+        (self.staged if staged else self.whole).replay()
+
+    def step_time(self):
+        return self.ew[0].elapsed_time(self.ew[1])
 
     def times(self):
         e = self.ev
@@ -300,20 +311,36 @@ def warm(gstep, warmup, torch, flush):
     for _ in range(warmup):
         gstep.replay()
         flush.zero_()
+        gstep.replay(staged=True)
+        flush.zero_()
     torch.cuda.synchronize()
 
 
-def time_device_steps(gstep, steps, torch, flush):
-    """One graph replay per step; the event nodes inside the graph time each kernel. L2 is
-    flushed between steps (outside the events) and each step's times are read before the next."""
-    per_stage = []
+def time_whole_steps(gstep, steps, torch, flush):
+    """One replay of the whole-step graph per step; L2 is flushed between steps (outside the
+    events) and each step's time is read before the next."""
+    per_step = []
     for _ in range(steps):
         flush.zero_()
         gstep.replay()
         torch.cuda.synchronize()
+        per_step.append(gstep.step_time())
+    return np.array(per_step)
+
+
+def time_stages(gstep, steps, torch, flush):
+    """The per-kernel breakdown: replays of the staged graph, L2 flushed between steps."""
+    per_stage = []
+    for _ in range(steps):
+        flush.zero_()
+        gstep.replay(staged=True)
+        torch.cuda.synchronize()
         per_stage.append(gstep.times())
-    per_stage = np.array(per_stage)
-    return per_stage.sum(axis=1), per_stage
+    return np.array(per_stage)
+
+
+def time_device_steps(gstep, steps, torch, flush):
+    return time_whole_steps(gstep, steps, torch, flush), time_stages(gstep, steps, torch, flush)
 
 
 def time_e2e(path, steps, warmup, torch):
@@ -522,11 +549,12 @@ def run_gpu(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    per_step, per_stage = time_device_steps(gstep, args.steps, torch, flush)
+    per_step = time_whole_steps(gstep, args.steps, torch, flush)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - t_wall0
+    per_stage = time_stages(gstep, args.steps, torch, flush)
     # keep the GPU busy a little longer so the sampler sees the clocks under this load
     t_end = time.perf_counter() + max(0.0, 1.0 - wall)
     while time.perf_counter() < t_end:
@@ -602,8 +630,9 @@ def run_gpu(args, rank, world, local):
             "config": {"workload": workload_label(base, K), "K": K, "T_total": wl.T_total, "M_kept": path.M,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "flushed between timed steps (256 MB write, outside the per-step events)",
-                       "timing": ("step captured in a CUDA graph with timing-event nodes between the kernels "
-                                  "(the launching stream); mean over steps; max over ranks")},
+                       "timing": ("step captured in a CUDA graph (events only around the step, kernels chained "
+                                  "by programmatic dependent launch); per-kernel times from a second graph with "
+                                  "events between the kernels, on the launching stream; mean over steps; max over ranks")},
             "roofline": roof,
             "stages": stages,
             "select_plus_gather": {"us": sel_gather_us, "achieved_gbs": sg_bytes / (sel_gather_us * 1e-6) / 1e9,

@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
   // ---- work item: heaviest (last) query tiles first ----
   const int item = blockIdx.x;
   const int hp = item % p.pairs;
@@ -521,9 +523,8 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
   const long long grid = static_cast<long long>(p.n_qt_max) * p.B * p.pairs;
   if (grid == 0) return TG_OK;
   if (grid > 0x7FFFFFFFLL) return TG_ERR_UNSUPPORTED;
-  gated_attention_kernel<D><<<static_cast<int>(grid), kThreads, C::kSmemBytes, stream>>>(
-      tm_q, tm_k, tm_v, p);
-  return tg_host::record_cuda(cudaGetLastError());
+  return tg_host::record_cuda(tg_host::launch_pdl(gated_attention_kernel<D>, dim3(static_cast<int>(grid)),
+                                                  dim3(kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, p));
 }
 
 }  // namespace

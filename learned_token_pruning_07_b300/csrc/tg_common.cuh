@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/tokengate.h"
 
 namespace tg {
@@ -27,6 +29,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: every kernel is launched so that it may start while the
+// previous kernel on the stream finishes. It waits here before reading anything an earlier
+// kernel may have written (the wait returns once the earlier grid has completed and its
+// writes are visible), and lets the next kernel start launching once all of its own CTAs
+// are running.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -286,6 +302,24 @@ bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64
                       const uint64_t *strides_bytes, const uint32_t *box,
                       CUtensorMapSwizzle swizzle);
 uint64_t wait_limit_ns();
+
+// Launch `kernel` on `stream` with programmatic stream serialization, so its launch and
+// prologue can overlap the previous kernel's tail (the kernel calls tg::pdl_wait() first).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 uint64_t drain_limit_ns();
 int32_t withhold_mask();
 int num_sms();

@@ -43,6 +43,8 @@ __device__ __forceinline__ void st_cs_v4(uint4 *p, uint4 v) {
 }
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nvec = p.d >> 3;  // 16-byte vectors per row
   const int stride = gridDim.x * kGatherWarps;
@@ -107,6 +109,8 @@ struct RopeParams {
 };
 
 __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeParams p) {
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
   int M = p.capacity;
   if (p.cu_kept) M = max(0, min(p.cu_kept[p.B], p.capacity));
   const int half = p.d_h >> 1;
@@ -147,8 +151,7 @@ tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
   int grid = (capacity + kGatherWarps - 1) / kGatherWarps;
   if (grid > num_sms() * 8) grid = num_sms() * 8;
   (void)rows_per_wave;
-  gather_kernel<<<grid, kGatherThreads, 0, stream>>>(p);
-  return record_cuda(cudaGetLastError());
+  return record_cuda(launch_pdl(gather_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, p));
 }
 
 tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
@@ -169,8 +172,7 @@ tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, i
   const long long total = static_cast<long long>(capacity) * half;
   long long grid = (total + 255) / 256;
   if (grid > num_sms() * 16) grid = num_sms() * 16;
-  rope_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(p);
-  return record_cuda(cudaGetLastError());
+  return record_cuda(launch_pdl(rope_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, stream, p));
 }
 
 }  // namespace tg_host

@@ -132,6 +132,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     tg::tmem_alloc(tmem_slot, kTmemCols);
     tg::tmem_relinquish();
   }
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
   for (int i = threadIdx.x; i < p.d_g; i += kThreads) {
     s_w2[i] = tg::bf16_bits_to_float(p.w2[i]);
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
@@ -337,8 +339,8 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
   int pairs = num_sms() / kPair;
   if (pairs > n_pairs) pairs = n_pairs;
-  gate_score_kernel<<<pairs * kPair, kThreads, L.total, stream>>>(tm_h, tm_w, p);
-  return record_cuda(cudaGetLastError());
+  return record_cuda(launch_pdl(gate_score_kernel, dim3(pairs * kPair), dim3(kThreads), L.total,
+                                stream, tm_h, tm_w, p));
 }
 
 }  // namespace tg_host

@@ -154,6 +154,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   const int b = blockIdx.x / kCluster;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
 
   // ---- this sequence's bounds (uniform across the cluster) ----
   const int start = p.cu_seqlens[b];
@@ -462,8 +464,7 @@ tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return record_cuda(e);
-  topk_select_kernel<<<B * kCluster, kThreads, smem, stream>>>(p);
-  return record_cuda(cudaGetLastError());
+  return record_cuda(launch_pdl(topk_select_kernel, dim3(B * kCluster), dim3(kThreads), smem, stream, p));
 }
 
 }  // namespace tg_host
