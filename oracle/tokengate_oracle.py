@@ -34,6 +34,11 @@ Readings where the pages leave a step open (each is listed in the design notes):
 Parity status of each function: every function here is pinned by tests that do
 not re-derive it from its own formula (library routines, closed forms, brute
 force, invariants). None is "parity unpinned".
+
+Readings for the exact gate form (normalize_scores, gated_attention_eq8): eps of
+the RMS normalisation is a parameter (default 1e-6; the pages give none); m_i is
+the number of retained keys query i sees (its index in the kept sequence + 1) and
+p_i the number of positions it originally saw (its original position + 1).
 """
 from __future__ import annotations
 
@@ -206,6 +211,68 @@ def gated_attention_weights_eq5(Q: np.ndarray, K: np.ndarray, g: Optional[np.nda
         w = w * np.power(np.asarray(g[: i + 1], dtype=np.float64), beta)
     total = w.sum()
     return w / total if total > 0 else np.zeros_like(w)
+
+
+# ---------------------------------------------------------------------------
+# The paper's exact gate form (deep dive section 3.1 Eq. (3); section 3.2 Eqs. (6)-(8)):
+# sequence-RMS-normalised scores, a per-head softplus gain on the score bias and a per-query
+# temperature from the pruning ratio.
+# ---------------------------------------------------------------------------
+
+def normalize_scores(s: np.ndarray, instr_mask: np.ndarray, cu_seqlens: Sequence[int],
+                     eps: float = 1e-6) -> np.ndarray:
+    """Eq. (3): b_j = b~_j / sqrt(mean over the sequence's prunable rows of b~^2 + eps), and
+    b_j = 0 on the non-prunable rows. A sequence with no prunable row has b = 0 throughout."""
+    s = np.asarray(s, dtype=np.float64)
+    b = np.zeros_like(s)
+    for i in range(len(cu_seqlens) - 1):
+        a, e = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+        doc = [j for j in range(a, e) if instr_mask[j] == 0]
+        if not doc:
+            continue
+        ms = sum(s[j] * s[j] for j in doc) / len(doc)
+        for j in doc:
+            b[j] = s[j] / math.sqrt(ms + eps)
+    return b
+
+
+def query_temperature(temp: float, m: int, p: int) -> float:
+    """Eq. (7): tau_i = softplus(sigma) * log m_i / log max(2, p_i), with softplus(sigma)
+    passed in as `temp`; m_i = retained keys query i sees, p_i = positions it originally saw."""
+    return float(temp) * math.log(m) / math.log(max(2, p))
+
+
+def gated_attention_eq8(Q: np.ndarray, K: np.ndarray, V: np.ndarray, b: Optional[np.ndarray],
+                        pos: np.ndarray, cu_kept: Sequence[int], gain: Sequence[float],
+                        temp: Sequence[float], rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Eq. (8): o_i = sum_{j<=i} softmax_j[tau_i (q_i.k_j / sqrt(d_h) + gain_h b_j)] v_j.
+
+    gain_h = softplus(gamma_h) (>= 0), tau_i from Eq. (7) with temp_h = softplus(sigma_h).
+    Query i of a sequence starting at kept row `start` sees m_i = i - start + 1 retained keys
+    and originally saw p_i = pos_i + 1 positions (pos holds the original position ids).
+    b None means no score bias. Layouts and `rows` as in gated_attention; two passes per row.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    M, H_q, d_h = Q.shape
+    group = H_q // K.shape[1]
+    cu = np.asarray(cu_kept, dtype=np.int64)
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), H_q, d_h), dtype=np.float64)
+    bias = np.zeros(M) if b is None else np.asarray(b, dtype=np.float64)
+    for n, i in enumerate(rows):
+        seq = int(np.searchsorted(cu, i, side="right") - 1)
+        start = int(cu[seq])
+        keys = np.arange(start, i + 1)
+        for h in range(H_q):
+            kv = h // group
+            tau = query_temperature(temp[h], i - start + 1, int(pos[i]) + 1)
+            z = (K[keys, kv, :] @ Q[i, h, :]) / math.sqrt(d_h)
+            logits = tau * (z + float(gain[h]) * bias[keys])
+            w = np.exp(logits - logits.max())
+            out[n, h, :] = (w / w.sum()) @ V[keys, kv, :]
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -60,8 +60,24 @@ def main():
             "9": [0, 1, 2, 3, 4, 5, 6, 7],
         },
     }
+    norm = {
+        "source": "TokenGate deep dive (agientry.com), section 3.1, Eq. (3): b_j = b~_j / sqrt(mean over P "
+                  "of b~^2 + eps), b_j = 0 on N; section 3.2, Eq. (7): tau_i = softplus(sigma) log m_i / "
+                  "log max(2, p_i)",
+        "derivation": "Two sequences. Sequence 0: raw scores (3, 4, 9) with row 2 non-prunable; mean of squares "
+                      "over P = (9 + 16)/2 = 12.5, so b = (3, 4)/sqrt(12.5) = (0.6 sqrt 2, 0.8 sqrt 2) and b_2 = 0. "
+                      "Sequence 1: raw scores (-2, 2, 2, -2), all prunable; mean square 4, so b = (-1, 1, 1, -1). "
+                      "eps = 0. Temperatures with softplus(sigma) = 1.5: (m, p) = (1, 1) -> 0; (2, 2) -> 1.5; "
+                      "(2, 4) -> 1.5 ln 2 / ln 4 = 0.75; (3, 9) -> 1.5 ln 3 / ln 9 = 0.75.",
+        "s": [3.0, 4.0, 9.0, -2.0, 2.0, 2.0, -2.0],
+        "instr_mask": [0, 0, 1, 0, 0, 0, 0],
+        "cu_seqlens": [0, 3, 7],
+        "b": [0.6 * math.sqrt(2.0), 0.8 * math.sqrt(2.0), 0.0, -1.0, 1.0, 1.0, -1.0],
+        "temp": 1.5,
+        "tau_cases": [[1, 1, 0.0], [2, 2, 1.5], [2, 4, 0.75], [3, 9, 0.75]],
+    }
     for name, obj in (("gate_score_closed_form.json", gate), ("attention_zero_logits.json", att),
-                      ("select_worked_example.json", sel)):
+                      ("select_worked_example.json", sel), ("normalized_scores_closed_form.json", norm)):
         with open(os.path.join(HERE, name), "w") as f:
             json.dump(obj, f, indent=1)
 

@@ -349,6 +349,119 @@ def test_attention_sequences_are_independent_and_rows_subset():
 
 
 # ---------------------------------------------------------------------------
+# The paper's exact gate form: Eq. (3) normalisation, Eq. (7) temperature, Eq. (8) attention
+# ---------------------------------------------------------------------------
+
+def test_normalize_scores_closed_form():
+    fx = _golden("normalized_scores_closed_form.json")
+    b = O.normalize_scores(np.array(fx["s"]), np.array(fx["instr_mask"]), fx["cu_seqlens"], eps=0.0)
+    np.testing.assert_allclose(b, fx["b"], rtol=0, atol=1e-15)
+    for m, p, want in fx["tau_cases"]:
+        assert abs(O.query_temperature(fx["temp"], m, p) - want) < 1e-15
+
+
+def test_normalize_scores_invariants():
+    rng = np.random.default_rng(31)
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(40, 0, 25), instr_lens=(6, 3, 0), instr_where="scattered")
+    mask = I.make_instr_mask(wl)
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    s = rng.standard_normal(wl.T_total) * 3.0
+    b = O.normalize_scores(s, mask, cu, eps=0.0)
+    assert np.all(b[mask == 1] == 0.0)
+    assert np.all(b[cu[1]:cu[2]] == 0.0)                      # no prunable rows: nothing to scale
+    for i in (0, 2):
+        doc = [j for j in range(cu[i], cu[i + 1]) if mask[j] == 0]
+        assert abs(np.mean(b[doc] ** 2) - 1.0) < 1e-12          # unit RMS over P
+        assert np.array_equal(np.argsort(-s[doc], kind="stable"), np.argsort(-b[doc], kind="stable"))
+    np.testing.assert_allclose(O.normalize_scores(7.5 * s, mask, cu, eps=0.0), b, rtol=1e-12)
+
+
+def _sdpa_eq8_rows(Q, K, V, b, pos, cu, gain, temp):
+    """torch CPU fp64 scaled_dot_product_attention, one query row at a time: scale tau_i/sqrt(d_h)
+    and additive mask tau_i * gain_h * b_j over the row's visible keys."""
+    M, H_q, d_h = Q.shape
+    group = H_q // K.shape[1]
+    out = torch.zeros(M, H_q, d_h, dtype=torch.float64)
+    for i in range(M):
+        seq = int(np.searchsorted(cu, i, side="right") - 1)
+        a = int(cu[seq])
+        m, p = i - a + 1, int(pos[i]) + 1
+        for h in range(H_q):
+            tau = temp[h] * math.log(m) / math.log(max(2, p))
+            q = torch.from_numpy(Q[i:i + 1, h][None])                       # [1, 1, d]
+            k = torch.from_numpy(K[a:i + 1, h // group][None])              # [1, m, d]
+            v = torch.from_numpy(V[a:i + 1, h // group][None])
+            mask = torch.from_numpy(tau * gain[h] * np.asarray(b[a:i + 1], np.float64))[None, None, :]
+            o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=tau / math.sqrt(d_h))
+            out[i, h] = o[0, 0]
+    return out.numpy()
+
+
+def _eq8_case(seed, lens):
+    rng = np.random.default_rng(seed)
+    Q, K, V, _, cu, _, _ = _rand_attn(seed, lens)
+    M = Q.shape[0]
+    b = rng.standard_normal(M)
+    pos = np.zeros(M, dtype=np.int64)
+    for i in range(len(lens)):                                # strictly increasing original ids with gaps
+        a, e = int(cu[i]), int(cu[i + 1])
+        pos[a:e] = np.cumsum(rng.integers(1, 6, e - a)) - 1
+    gain = rng.uniform(0.2, 1.5, Q.shape[1])
+    temp = rng.uniform(0.5, 1.5, Q.shape[1])
+    return Q, K, V, b, pos, cu, gain, temp
+
+
+@pytest.mark.parametrize("lens", [(13,), (4, 1, 17)])
+def test_eq8_attention_matches_rowwise_sdpa(lens):
+    Q, K, V, b, pos, cu, gain, temp = _eq8_case(41, lens)
+    got = O.gated_attention_eq8(Q, K, V, b, pos, cu, gain, temp)
+    ref = _sdpa_eq8_rows(Q, K, V, b, pos, cu, gain, temp)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_eq8_without_pruning_reduces_to_the_log_gate_form():
+    # m_i = p_i (nothing pruned) and softplus(sigma) = 1 give tau_i = 1 (row 0 sees only itself);
+    # gain_h * b_j is then the log-bias beta_h ln g_j with g = exp(b), beta = gain
+    Q, K, V, b, _, cu, gain, _ = _eq8_case(42, (11, 5))
+    pos = np.concatenate([np.arange(11), np.arange(5)])
+    got = O.gated_attention_eq8(Q, K, V, b, pos, cu, gain, np.ones(Q.shape[1]))
+    ref = O.gated_attention(Q, K, V, np.exp(b), cu, np.ones(Q.shape[1]), gain)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def _planted_eq8(kind, Q, K, V, b, pos, cu, gain, temp):
+    """gated_attention_eq8 with one planted mistake, for the pin below."""
+    M, H_q, d_h = Q.shape
+    group = H_q // K.shape[1]
+    out = np.zeros((M, H_q, d_h))
+    for i in range(M):
+        a = int(cu[np.searchsorted(cu, i, side="right") - 1])
+        keys = np.arange(a, i + 1)
+        m, p = i - a + 1, int(pos[i]) + 1
+        if kind == "p_without_plus_one":
+            p -= 1
+        for h in range(H_q):
+            tau = temp[h] * math.log(m) / math.log(max(2, p))
+            z = (K[keys, h // group] @ Q[i, h]) / math.sqrt(d_h)
+            if kind == "tau_on_logit_only":
+                logits = tau * z + gain[h] * b[keys]
+            else:
+                logits = tau * (z + gain[h] * b[keys])
+            w = np.exp(logits - logits.max())
+            out[i, h] = (w / w.sum()) @ V[keys, h // group]
+    return out
+
+
+@pytest.mark.parametrize("kind", ["tau_on_logit_only", "p_without_plus_one"])
+def test_planted_eq8_mistakes_fail_the_rowwise_pin(kind):
+    Q, K, V, b, pos, cu, gain, temp = _eq8_case(43, (14,))
+    ref = _sdpa_eq8_rows(Q, K, V, b, pos, cu, gain, temp)
+    assert np.allclose(_planted_eq8("none", Q, K, V, b, pos, cu, gain, temp), ref, rtol=1e-10, atol=1e-12)
+    wrong = _planted_eq8(kind, Q, K, V, b, pos, cu, gain, temp)
+    assert not np.allclose(wrong, ref, rtol=1e-6, atol=1e-8)
+
+
+# ---------------------------------------------------------------------------
 # RoPE
 # ---------------------------------------------------------------------------
 
