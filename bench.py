@@ -481,6 +481,46 @@ def long_context(torch, flush, steps):
             "attention_time_ratio_full_over_pruned": full_ms / pruned_attn_ms}
 
 
+def paper_form(path, torch, flush, steps):
+    """The paper's exact gate form on the bench batch: score normalisation (Eq. (3)) over the
+    step's scores, and Eq. (8) attention with the Eq. (7) temperature over the kept rows."""
+    from learned_token_pruning_07_b300 import binding as tg
+    wl = path.wl
+    b_all = torch.empty_like(path.s)
+    rng = np.random.default_rng(wl.seed + 5)
+    gain = rng.uniform(0.5, 1.5, wl.H_q).astype(np.float32)
+    temp = rng.uniform(0.8, 1.2, wl.H_q).astype(np.float32)
+    d = path.d
+
+    def norm():
+        tg.normalize_scores(path.s, d["cu"], b_all, instr_mask=d["mask"], status=path.status)
+
+    def attn():
+        tg.gated_attention_eq8(d["Q"], d["K"], d["V"], path.cu_kept, path.pos_kept[:path.M], gain, temp, path.O,
+                               max_seqlen=path.max_seqlen, b=path.g_kept[:path.M], status=path.status)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, min(steps, 20))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1000.0)
+        return float(np.median(ts))
+
+    norm_us, attn_us = timed(norm), timed(attn)
+    assert tg.read_device_status(path.status) == 0, "device reported an error"
+    flops = stage_work(wl, path.K, path.kept_lens)["gated_attention"]["flops"]
+    return {"normalize_scores_us": norm_us, "attention_eq8_us": attn_us,
+            "attention_eq8_tflops": flops / (attn_us * 1e-6) / 1e12,
+            "note": "single launches with events around each (launch gap included), L2 flushed before each"}
+
+
 def workload_label(wl, K):
     docs = wl.doc_lens if wl.B > 1 else wl.doc_lens[0]
     ins = wl.instr_lens if wl.B > 1 else wl.instr_lens[0]
@@ -616,6 +656,7 @@ def run_gpu(args, rank, world, local):
                 del g2, p2
                 torch.cuda.empty_cache()
 
+    paper = paper_form(path, torch, flush, args.steps) if rank == 0 else None
     longctx = long_context(torch, flush, args.steps) if (args.long_context and rank == 0) else None
 
     cpu = None
@@ -647,6 +688,8 @@ def run_gpu(args, rank, world, local):
         }
         if sweep:
             line["sweep"] = sweep
+        if paper:
+            line["paper_form"] = paper
         if longctx:
             line["long_context"] = longctx
         print(json.dumps(line), flush=True)

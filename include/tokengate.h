@@ -181,6 +181,40 @@ TG_API tg_status tg_apply_rope(uint16_t *X, const int32_t *pos, const int32_t *c
                         tg_stream_t stream);
 
 /*
+ * tg_normalize_scores — sequence-axis RMS normalisation of the gate scores (deep dive section
+ *   3.1, Eq. (3)): b_j = s_j / sqrt(mean over the sequence's prunable rows of s^2 + eps), and
+ *   b_j = 0 on non-prunable rows. A sequence without prunable rows gets b = 0. The order of
+ *   the prunable scores is unchanged, so top-K may select from s or from b alike.
+ *   s [device] fp32 [T_total] (as written by tg_gate_score); instr_mask [device] uint8 or NULL;
+ *   cu_seqlens [device] int32 [B+1]; eps: host, finite, >= 0 (the pages give none; 1e-6 is the
+ *   usual choice). b_out [device] fp32 [T_total]. status [device] int32 word (TG_DEV_BAD_SEQLENS).
+ *   Limits: 1 <= B <= 1024. The per-sequence sum runs in a fixed order (deterministic).
+ */
+TG_API tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
+                              int32_t B, int32_t T_total, float eps, float *b_out, int32_t *status,
+                              tg_stream_t stream);
+
+/*
+ * tg_gated_attention_eq8 — the operative token-gated attention of the deep dive, section 3.2,
+ *   Eq. (8), with the pruning-ratio temperature of Eq. (7):
+ *     o_i = sum_{j <= i} softmax_j[ tau_i (q_i.k_j / sqrt(d_h) + gain_h b_j) ] v_j,
+ *     tau_i = temp_h ln(m_i) / ln(max(2, p_i)),
+ *   m_i = number of retained keys query i sees (its index in the kept sequence + 1),
+ *   p_i = number of positions it originally saw (its original position id + 1).
+ *   gain_h = softplus(gamma_h) and temp_h = softplus(sigma_h) are passed already transformed.
+ *   b   [device] fp32 [M]: normalised scores of the kept rows (tg_normalize_scores, gathered by
+ *       tg_gather_kept), or NULL for no score bias.
+ *   pos [device] int32 [M]: original position ids of the kept rows (tg_gather_kept's pos_kept).
+ *   gain, temp [host] fp32 [H_q], finite and >= 0.
+ *   Other arguments, layouts, shapes and errors as tg_gated_attention.
+ */
+TG_API tg_status tg_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                 int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q,
+                                 int32_t H_kv, int32_t d_h, const float *gain, const float *temp,
+                                 uint16_t *O, int32_t *status, tg_stream_t stream);
+
+/*
  * tg_read_device_status — synchronise `stream`, copy the device status word to *out and
  *   translate it: 0 -> TG_OK, TG_DEV_TIMEOUT -> TG_ERR_DEVICE_TIMEOUT, TG_DEV_CAPACITY ->
  *   TG_ERR_CAPACITY, any other bit -> TG_ERR_DEVICE. *out receives the raw bits.

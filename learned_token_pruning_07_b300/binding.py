@@ -34,6 +34,8 @@ SIGNATURES = {
     "tg_gate_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
                                  _P, _P, _P, _P, _P, _P]),
     "tg_apply_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "tg_normalize_scores": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P]),
+    "tg_gated_attention_eq8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tg_read_device_status": (_I, [_P, _P, _P]),
     "tg_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "tg_set_test_withhold": (_I, [_I]),
@@ -136,6 +138,27 @@ def gated_attention(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, sta
                                    _ptr(status), _stream(stream))
     del tau_a, beta_a
     _check("tg_gated_attention", st)
+
+
+def normalize_scores(s, cu_seqlens, b_out, instr_mask=None, eps: float = 1e-6, status=None, stream=None):
+    B = cu_seqlens.numel() - 1
+    st = load().tg_normalize_scores(_ptr(s), _ptr(instr_mask), _ptr(cu_seqlens), B, s.numel(), float(eps),
+                                    _ptr(b_out), _ptr(status), _stream(stream))
+    _check("tg_normalize_scores", st)
+
+
+def gated_attention_eq8(Q, K, V, cu_kept, pos, gain, temp, O, max_seqlen: int, b=None, status=None,
+                        stream=None):
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    B = cu_kept.numel() - 1
+    gain_a, gain_p = _host_f32(gain)
+    temp_a, temp_p = _host_f32(temp)
+    st = load().tg_gated_attention_eq8(_ptr(Q), _ptr(K), _ptr(V), _ptr(b), _ptr(pos), _ptr(cu_kept), B, M,
+                                       int(max_seqlen), H_q, H_kv, d_h, gain_p, temp_p, _ptr(O), _ptr(status),
+                                       _stream(stream))
+    del gain_a, temp_a
+    _check("tg_gated_attention_eq8", st)
 
 
 def gate_prune_layer(h, cu_seqlens, W1, w2, K: int, s_out, g_out, kept_idx, cu_kept, h_kept,

@@ -24,6 +24,15 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                                  int32_t *status, cudaStream_t stream);
+tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                     const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                     int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q,
+                                     int32_t H_kv, int32_t d_h, const float *gain,
+                                     const float *temp, uint16_t *O, int32_t *status,
+                                     cudaStream_t stream);
+tg_status launch_normalize_scores(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
+                                  int32_t B, int32_t T, float eps, float *b_out, int32_t *status,
+                                  cudaStream_t stream);
 }  // namespace tg_host
 
 namespace {
@@ -110,6 +119,35 @@ tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_
   if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
   return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
                                          d_h, tau, beta, O, status, S(stream));
+}
+
+tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
+                              int32_t B, int32_t T_total, float eps, float *b_out, int32_t *status,
+                              tg_stream_t stream) {
+  if (!s || !cu_seqlens || !b_out) return TG_ERR_INVALID_ARG;
+  if (B < 1 || T_total < 0 || !std::isfinite(eps) || eps < 0.0f) return TG_ERR_INVALID_ARG;
+  if (B > kMaxSelectB) return TG_ERR_UNSUPPORTED;
+  if (T_total == 0) return TG_OK;
+  return tg_host::launch_normalize_scores(s, instr_mask, cu_seqlens, B, T_total, eps, b_out, status,
+                                          S(stream));
+}
+
+tg_status tg_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                 int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q,
+                                 int32_t H_kv, int32_t d_h, const float *gain, const float *temp,
+                                 uint16_t *O, int32_t *status, tg_stream_t stream) {
+  if (!Q || !K || !V || !pos || !cu_kept || !gain || !temp || !O) return TG_ERR_INVALID_ARG;
+  if (B < 1 || M_capacity < 0 || max_seqlen < 0 || H_q < 1 || H_kv < 1 || d_h < 1)
+    return TG_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TG_ERR_INVALID_ARG;
+  for (int h = 0; h < H_q && h < 128; ++h) {
+    if (!std::isfinite(gain[h]) || gain[h] < 0.0f) return TG_ERR_INVALID_ARG;
+    if (!std::isfinite(temp[h]) || temp[h] < 0.0f) return TG_ERR_INVALID_ARG;
+  }
+  if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
+  return tg_host::launch_gated_attention_eq8(Q, K, V, b, pos, cu_kept, B, M_capacity, max_seqlen, H_q,
+                                             H_kv, d_h, gain, temp, O, status, S(stream));
 }
 
 tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,

@@ -46,16 +46,24 @@ struct AttnCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 };
 
+// Two forms of the score bias and temperature (TokenGate deep dive, section 3.2):
+//   kLogGate: logit = tau_h q.k / sqrt(d_h) + beta_h ln g_j                 (Eq. (5) in log form)
+//   kEq8:     logit = tau_i (q.k / sqrt(d_h) + gain_h b_j),                  (Eq. (8))
+//             tau_i = temp_h ln(m_i) / ln(max(2, p_i))                        (Eq. (7))
+//             with m_i = i - start + 1 retained keys, p_i = pos_i + 1 original positions.
+enum { kLogGate = 0, kEq8 = 1 };
+
 struct AttnParams {
-  const float *g;
+  const float *g;            // kLogGate: gate values g_j; kEq8: normalised scores b_j (or NULL)
+  const int32_t *pos;        // kEq8: original position ids of the kept rows
   const int32_t *cu_kept;
   int32_t B, M_cap, max_seqlen, H_q, H_kv, group, heads_per_cta, pairs, n_qt_max;
   uint16_t *O;
   int32_t *status;
   uint64_t wait_limit, drain_limit;
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
-  float scale_log2[kMaxHeads];  // tau_h * log2(e) / sqrt(d_h)
-  float beta[kMaxHeads];
+  float scale_log2[kMaxHeads];  // kLogGate: tau_h * log2(e) / sqrt(d_h); kEq8: temp_h
+  float beta[kMaxHeads];        // kLogGate: beta_h; kEq8: gain_h * log2(e)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -100,7 +108,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gated_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -302,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // ---------------- bias producer: beta_h * log2(g) per key, both heads ----------------
+    // ---------------- bias producer: the per-key bias of each K/V tile, both heads ----------------
     if (p.g != nullptr) {
       const float beta0 = p.beta[h0];
       const float beta1 = n_tiles > 1 ? p.beta[h0 + 1] : 0.0f;
@@ -320,13 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int k = j * kBlockN + lane * 4 + i;
-          gv[i] = k < seq_len ? p.g[seq_start + k] : 1.0f;
+          gv[i] = k < seq_len ? p.g[seq_start + k] : (MODE == kEq8 ? 0.0f : 1.0f);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float lgv = lg2(gv[i]);
-          dst[lane * 4 + i] = beta0 == 0.0f ? 0.0f : beta0 * lgv;
-          dst[128 + lane * 4 + i] = beta1 == 0.0f ? 0.0f : beta1 * lgv;
+          // kLogGate: beta_h log2(g_j) (beta = 0 means g^0 = 1, a zero bias even where g = 0);
+          // kEq8: gain_h log2(e) b_j, the log2-unit score bias before the row's temperature
+          const float v = MODE == kEq8 ? gv[i] : lg2(gv[i]);
+          dst[lane * 4 + i] = beta0 == 0.0f ? 0.0f : beta0 * v;
+          dst[128 + lane * 4 + i] = beta1 == 0.0f ? 0.0f : beta1 * v;
         }
         tg::mbar_arrive(&bias_full[st]);
       }
@@ -343,7 +353,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t colS = t == 0 ? C::kColS0 : C::kColS1;
       const uint32_t colO = t == 0 ? C::kColO0 : C::kColO1;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-      const uint64_t scale2 = f2(scale, scale);
+      // kEq8: this row's temperature (Eq. (7)); rows past the sequence end are never stored
+      float tau_row = 1.0f;
+      if (MODE == kEq8) {
+        const int i_local = q0 + r;  // index of the query in its kept sequence
+        if (i_local < seq_len) {
+          const int m_i = i_local + 1;
+          const int p_i = p.pos[seq_start + i_local] + 1;
+          tau_row = scale * (logf(static_cast<float>(m_i)) / logf(static_cast<float>(max(2, p_i))));
+        }
+      }
+      // kLogGate: x = s * scale + bias.  kEq8: x = tau_i * (s * log2(e) / sqrt(d_h) + bias)
+      const float c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+      const float s_mul = MODE == kEq8 ? (use_bias ? c1 : c1 * tau_row) : scale;
+      const uint64_t scale2 = f2(s_mul, s_mul);
+      const uint64_t tau2 = f2(tau_row, tau_row);
       float m_ref = -INFINITY;  // reference max (log2 units)
       float l = 0.0f;
       bool ok = true;
@@ -367,8 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) {
             const float4 bv = bias4[c];
             float a0, a1, a2, a3;
-            f2_split(f2_fma(f2(__uint_as_float(x[4 * c]), __uint_as_float(x[4 * c + 1])), scale2, f2(bv.x, bv.y)), a0, a1);
-            f2_split(f2_fma(f2(__uint_as_float(x[4 * c + 2]), __uint_as_float(x[4 * c + 3])), scale2, f2(bv.z, bv.w)), a2, a3);
+            uint64_t v01 = f2_fma(f2(__uint_as_float(x[4 * c]), __uint_as_float(x[4 * c + 1])), scale2, f2(bv.x, bv.y));
+            uint64_t v23 = f2_fma(f2(__uint_as_float(x[4 * c + 2]), __uint_as_float(x[4 * c + 3])), scale2, f2(bv.z, bv.w));
+            if (MODE == kEq8) {
+              v01 = f2_mul(v01, tau2);
+              v23 = f2_mul(v23, tau2);
+            }
+            f2_split(v01, a0, a1);
+            f2_split(v23, a2, a3);
             x[4 * c] = __float_as_uint(a0);
             x[4 * c + 1] = __float_as_uint(a1);
             x[4 * c + 2] = __float_as_uint(a2);
@@ -492,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int MODE>
 tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                              AttnParams &p, cudaStream_t stream) {
   using C = AttnCfg<D>;
@@ -516,14 +546,14 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
     if (!tg_host::encode_tmap_bf16(&tm_v, V, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(gated_attention_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(gated_attention_kernel<D, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return tg_host::record_cuda(e);
   const long long grid = static_cast<long long>(p.n_qt_max) * p.B * p.pairs;
   if (grid == 0) return TG_OK;
   if (grid > 0x7FFFFFFFLL) return TG_ERR_UNSUPPORTED;
-  return tg_host::record_cuda(tg_host::launch_pdl(gated_attention_kernel<D>, dim3(static_cast<int>(grid)),
+  return tg_host::record_cuda(tg_host::launch_pdl(gated_attention_kernel<D, MODE>, dim3(static_cast<int>(grid)),
                                                   dim3(kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, p));
 }
 
@@ -531,14 +561,14 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
 
 namespace tg_host {
 
-tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const int32_t *cu_kept, int32_t B,
-                                 int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
-                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
-                                 int32_t *status, cudaStream_t stream) {
-  if (M_cap == 0 || max_seqlen == 0) return TG_OK;
+namespace {
+
+AttnParams common_params(const float *bias_src, const int32_t *pos, const int32_t *cu_kept, int32_t B,
+                         int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv, uint16_t *O,
+                         int32_t *status) {
   AttnParams p;
-  p.g = g;
+  p.g = bias_src;
+  p.pos = pos;
   p.cu_kept = cu_kept;
   p.B = B;
   p.M_cap = M_cap;
@@ -554,13 +584,43 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
   p.wait_limit = wait_limit_ns();
   p.drain_limit = drain_limit_ns();
   p.withhold = (withhold_mask() & TG_WITHHOLD_ATTENTION) != 0;
+  return p;
+}
+
+}  // namespace
+
+tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                 int32_t *status, cudaStream_t stream) {
+  if (M_cap == 0 || max_seqlen == 0) return TG_OK;
+  AttnParams p = common_params(g, nullptr, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale_log2[h] = h < H_q ? tau[h] * log2e / std::sqrt(static_cast<float>(d_h)) : 0.0f;
     p.beta[h] = h < H_q ? beta[h] : 0.0f;
   }
-  if (d_h == 128) return launch_attention_d<128>(Q, K, V, p, stream);
-  if (d_h == 64) return launch_attention_d<64>(Q, K, V, p, stream);
+  if (d_h == 128) return launch_attention_d<128, kLogGate>(Q, K, V, p, stream);
+  if (d_h == 64) return launch_attention_d<64, kLogGate>(Q, K, V, p, stream);
+  return TG_ERR_UNSUPPORTED;
+}
+
+tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                     const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                     int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q,
+                                     int32_t H_kv, int32_t d_h, const float *gain,
+                                     const float *temp, uint16_t *O, int32_t *status,
+                                     cudaStream_t stream) {
+  if (M_cap == 0 || max_seqlen == 0) return TG_OK;
+  AttnParams p = common_params(b, pos, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
+  const float log2e = 1.4426950408889634f;
+  for (int h = 0; h < kMaxHeads; ++h) {
+    p.scale_log2[h] = h < H_q ? temp[h] : 0.0f;
+    p.beta[h] = h < H_q ? gain[h] * log2e : 0.0f;
+  }
+  if (d_h == 128) return launch_attention_d<128, kEq8>(Q, K, V, p, stream);
+  if (d_h == 64) return launch_attention_d<64, kEq8>(Q, K, V, p, stream);
   return TG_ERR_UNSUPPORTED;
 }
 

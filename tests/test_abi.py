@@ -21,7 +21,7 @@ def lib():
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -95,3 +95,27 @@ def test_test_withhold_hook_validates_its_mask(lib):
     assert lib.tg_set_test_withhold(binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION) == binding.TG_OK
     assert lib.tg_set_test_withhold(4) == binding.TG_ERR_INVALID_ARG
     assert lib.tg_set_test_withhold(0) == binding.TG_OK
+
+
+def test_normalize_scores_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.tg_normalize_scores(None, None, p, 1, 8, 1e-6, p, None, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_normalize_scores(p, None, p, 0, 8, 1e-6, p, None, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_normalize_scores(p, None, p, 1, 8, -1.0, p, None, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_normalize_scores(p, None, p, 1, 8, float("nan"), p, None, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_normalize_scores(p, None, p, 2000, 8, 1e-6, p, None, None) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_eq8_attention_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    ones = np.ones(16, np.float32)
+    neg = ones.copy()
+    neg[3] = -0.5
+    f = lambda a: a.ctypes.data
+    call = lambda pos, gain, temp, hq=16, hkv=8, dh=128: lib.tg_gated_attention_eq8(
+        p, p, p, None, pos, p, 1, 100, 100, hq, hkv, dh, gain, temp, p, None, None)
+    assert call(None, f(ones), f(ones)) == binding.TG_ERR_INVALID_ARG          # positions required
+    assert call(p, f(neg), f(ones)) == binding.TG_ERR_INVALID_ARG              # gain >= 0
+    assert call(p, f(ones), f(neg)) == binding.TG_ERR_INVALID_ARG              # temperature >= 0
+    assert call(p, f(ones), f(ones), dh=96) == binding.TG_ERR_UNSUPPORTED
+    assert call(p, f(ones), f(ones), hq=12, hkv=8) == binding.TG_ERR_UNSUPPORTED
