@@ -53,15 +53,26 @@ import numpy as np
 # a sigmoid (see module docstring).
 # ---------------------------------------------------------------------------
 
+def rms_norm(a: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """LN_2 of Eq. (1) in the RMSNorm form of the Qwen3 family: a / sqrt(mean(a^2) + eps) * w."""
+    a = np.asarray(a, dtype=np.float64)
+    rms = np.sqrt(np.mean(a * a, axis=-1, keepdims=True) + eps)
+    return a / rms * np.asarray(weight, dtype=np.float64)
+
+
 def gate_score(h: np.ndarray, W1: np.ndarray, w2: np.ndarray, instr_mask: np.ndarray,
-               b1: Optional[np.ndarray] = None, b2: float = 0.0):
+               b1: Optional[np.ndarray] = None, b2: float = 0.0,
+               ln_weight: Optional[np.ndarray] = None, ln_eps: float = 1e-6):
     """Score every row: u = W1 h (+ b1), a = SiLU(u), s = w2 . a (+ b2), g = sigmoid(s).
 
     h [T, d], W1 [d_g, d], w2 [d_g], instr_mask [T] (1 = non-prunable).
     Returns (s [T], g [T]) in float64; g = 1 on non-prunable rows.
     Deep dive section 3.1, Eq. (3): b~_j = MLP(a~_j); the tokens in the
-    non-prunable set carry no bias (read here as g_j = 1).
+    non-prunable set carry no bias (read here as g_j = 1). With ln_weight given,
+    h is the post-attention residual a^L and the MLP reads LN_2(a^L) (Eq. (1)).
     """
+    if ln_weight is not None:
+        h = rms_norm(h, ln_weight, ln_eps)
     h = np.asarray(h, dtype=np.float64)
     W1 = np.asarray(W1, dtype=np.float64)
     w2 = np.asarray(w2, dtype=np.float64)

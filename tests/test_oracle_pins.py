@@ -58,6 +58,23 @@ def test_gate_score_matches_torch_mlp(with_bias):
     np.testing.assert_allclose(g, ref_g.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def test_gate_score_with_rmsnorm_matches_torch():
+    # LN_2 (Eq. (1)) as RMSNorm, then the score MLP: torch CPU fp64 F.rms_norm + F.linear / F.silu
+    wl = I.WORKLOADS["tiny"]
+    gi = I.make_gate_inputs(wl)
+    h = I.bf16_bits_to_f64(gi["h"]) * 3.0 + 0.5
+    W1, w2 = I.bf16_bits_to_f64(gi["W1"]), I.bf16_bits_to_f64(gi["w2"])
+    ln_w = np.random.default_rng(9).uniform(0.5, 1.5, wl.d)
+    s, g = O.gate_score(h, W1, w2, gi["instr_mask"], ln_weight=ln_w, ln_eps=1e-6)
+    x = F.rms_norm(torch.from_numpy(h), (wl.d,), torch.from_numpy(ln_w), 1e-6)
+    ref_s = F.linear(F.silu(F.linear(x, torch.from_numpy(W1))), torch.from_numpy(w2)[None, :]).squeeze(1)
+    np.testing.assert_allclose(s, ref_s.numpy(), rtol=1e-12, atol=1e-12)
+    # a row scaled by any c > 0 normalises to the same vector, so its score does not change
+    s2, _ = O.gate_score(h * 7.0, W1, w2, gi["instr_mask"], ln_weight=ln_w, ln_eps=0.0)
+    s3, _ = O.gate_score(h, W1, w2, gi["instr_mask"], ln_weight=ln_w, ln_eps=0.0)
+    np.testing.assert_allclose(s2, s3, rtol=1e-12, atol=1e-12)
+
+
 def test_gate_score_zero_initialised_mlp():
     # The score MLP starts at zero (deep dive section 3.1): every document token scores 0,
     # so g = sigmoid(0) = 1/2; instruction tokens carry g = 1.
