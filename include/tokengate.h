@@ -92,6 +92,30 @@ TG_API tg_status tg_gate_score(const uint16_t *h, int32_t T_total, int32_t d, co
                         tg_stream_t stream);
 
 /*
+ * tg_gate_score_rmsnorm — tg_gate_score with LN_2 fused in front of the score MLP (deep dive
+ *   section 2, Eq. (1): the gate scores the normalised post-attention residual
+ *   a~ = LN_2(a^L); in the Qwen3 family LN_2 is an RMSNorm with a weight w_ln):
+ *     u = W1 (w_ln * h / sqrt(mean_c h_c^2 + ln_eps)) (+ b1), then as tg_gate_score.
+ *   h is the raw residual a^L. W1_folded [device] bf16 [d_g, d] = W1 diag(w_ln) rounded to
+ *   bf16, as written by tg_fold_rmsnorm_weight; the kernel sums each row's squares while the
+ *   row streams through shared memory and scales the row's accumulator by 1/rms, so the
+ *   normalised activations never go to memory. ln_eps: host, finite, >= 0.
+ *   Other arguments, shapes and errors as tg_gate_score.
+ */
+TG_API tg_status tg_gate_score_rmsnorm(const uint16_t *h, int32_t T_total, int32_t d,
+                                const uint8_t *instr_mask, const uint16_t *W1_folded, const float *b1,
+                                const uint16_t *w2, float b2, int32_t d_g, float ln_eps, float *s_out,
+                                float *g_out, int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_fold_rmsnorm_weight — W1_out[k, c] = bf16(W1[k, c] * ln_weight[c]) (round to nearest
+ *   even), the weight tg_gate_score_rmsnorm takes. W1 [device] bf16 [d_g, d]; ln_weight
+ *   [device] bf16 [d]; W1_out [device] bf16 [d_g, d] (may not alias W1). Run once per weight.
+ */
+TG_API tg_status tg_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_weight, int32_t d_g,
+                                 int32_t d, uint16_t *W1_out, tg_stream_t stream);
+
+/*
  * tg_topk_select — the retained set (deep dive section 3.1, Eq. (4): S = topK_{j in P}(b_j)
  *   union N; section 3.4: the budget is clamped to |P| and the keep indices are built over
  *   the full sequence in original order).

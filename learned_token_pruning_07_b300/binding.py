@@ -28,6 +28,8 @@ SIGNATURES = {
     "tg_status_string": (ctypes.c_char_p, [_I]),
     "tg_last_cuda_error": (_I, []),
     "tg_gate_score": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P]),
+    "tg_gate_score_rmsnorm": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _I, _F, _P, _P, _P, _P]),
+    "tg_fold_rmsnorm_weight": (_I, [_P, _P, _I, _I, _P, _P]),
     "tg_topk_select": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "tg_gather_kept": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "tg_gated_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -106,6 +108,22 @@ def gate_score(h, W1, w2, s_out, g_out=None, instr_mask=None, b1=None, b2: float
     st = load().tg_gate_score(_ptr(h), T, d, _ptr(instr_mask), _ptr(W1), _ptr(b1), _ptr(w2), float(b2),
                               d_g, _ptr(s_out), _ptr(g_out), _ptr(status), _stream(stream))
     _check("tg_gate_score", st)
+
+
+def gate_score_rmsnorm(h, W1_folded, w2, s_out, g_out=None, instr_mask=None, b1=None, b2: float = 0.0,
+                       ln_eps: float = 1e-6, status=None, stream=None):
+    T, d = h.shape
+    d_g = W1_folded.shape[0]
+    st = load().tg_gate_score_rmsnorm(_ptr(h), T, d, _ptr(instr_mask), _ptr(W1_folded), _ptr(b1), _ptr(w2),
+                                      float(b2), d_g, float(ln_eps), _ptr(s_out), _ptr(g_out), _ptr(status),
+                                      _stream(stream))
+    _check("tg_gate_score_rmsnorm", st)
+
+
+def fold_rmsnorm_weight(W1, ln_weight, W1_out, stream=None):
+    d_g, d = W1.shape
+    _check("tg_fold_rmsnorm_weight", load().tg_fold_rmsnorm_weight(_ptr(W1), _ptr(ln_weight), d_g, d,
+                                                                     _ptr(W1_out), _stream(stream)))
 
 
 def topk_select(s, cu_seqlens, K: int, kept_idx, cu_kept, instr_mask=None, status=None, stream=None):

@@ -8,7 +8,9 @@ namespace tg_host {
 tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8_t *mask,
                             const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
                             int32_t d_g, float *s_out, float *g_out, int32_t *status,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool rmsnorm, float ln_eps);
+tg_status launch_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_w, int32_t d_g, int32_t d,
+                                     uint16_t *W1_out, cudaStream_t stream);
 tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
                              int32_t B, int32_t T, int32_t K, int32_t *kept_idx, int32_t capacity,
                              int32_t *cu_kept, int32_t *status, cudaStream_t stream);
@@ -80,7 +82,24 @@ tg_status tg_gate_score(const uint16_t *h, int32_t T_total, int32_t d, const uin
   tg_status st = check_gate_score(h, T_total, d, W1, w2, d_g, s_out, b2);
   if (st != TG_OK) return st;
   return tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, w2, b2, d_g, s_out, g_out,
-                                    status, S(stream));
+                                    status, S(stream), false, 0.0f);
+}
+
+tg_status tg_gate_score_rmsnorm(const uint16_t *h, int32_t T_total, int32_t d,
+                                const uint8_t *instr_mask, const uint16_t *W1_folded, const float *b1,
+                                const uint16_t *w2, float b2, int32_t d_g, float ln_eps, float *s_out,
+                                float *g_out, int32_t *status, tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1_folded, w2, d_g, s_out, b2);
+  if (st != TG_OK) return st;
+  if (!std::isfinite(ln_eps) || ln_eps < 0.0f) return TG_ERR_INVALID_ARG;
+  return tg_host::launch_gate_score(h, T_total, d, instr_mask, W1_folded, b1, w2, b2, d_g, s_out, g_out,
+                                    status, S(stream), true, ln_eps);
+}
+
+tg_status tg_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_weight, int32_t d_g, int32_t d,
+                                 uint16_t *W1_out, tg_stream_t stream) {
+  if (!W1 || !ln_weight || !W1_out || d_g <= 0 || d <= 0) return TG_ERR_INVALID_ARG;
+  return tg_host::launch_fold_rmsnorm_weight(W1, ln_weight, d_g, d, W1_out, S(stream));
 }
 
 tg_status tg_topk_select(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
@@ -164,7 +183,7 @@ tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8
     st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity, h_kept);
   if (st != TG_OK) return st;
   st = tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, w2, b2, d_g, s_out, g_out,
-                                  status, S(stream));
+                                  status, S(stream), false, 0.0f);
   if (st != TG_OK) return st;
   st = tg_host::launch_topk_select(s_out, instr_mask, cu_seqlens, B, T_total, K, kept_idx,
                                    capacity, cu_kept, status, S(stream));

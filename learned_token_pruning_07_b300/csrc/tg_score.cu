@@ -25,7 +25,8 @@ namespace {
 constexpr int kBM = 128;      // rows per tile = tensor-memory lanes
 constexpr int kBK = 64;       // d-elements per pipeline stage (one 128-byte swizzled row)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;      // warps 0 (TMA), 1 (MMA), 2-5 (epilogue)
+constexpr int kThreadsNorm = 320;  // + warps 6-9: row sums of squares for the fused RMSNorm
 constexpr int kMaxDg = 512;
 constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
@@ -33,6 +34,7 @@ constexpr int kPair = 2;  // CTAs of a cluster: neighbouring row tiles that shar
 
 struct ScoreParams {
   int32_t T, d, d_g, n_items, item_n, n_tiles, KT;
+  float ln_eps;  // fused RMSNorm (LN_2 of the residual): 1 / sqrt(mean(h^2) + ln_eps) per row
   const float *b1;
   const uint16_t *w2;
   float b2;
@@ -45,7 +47,7 @@ struct ScoreParams {
 };
 
 struct SmemLayout {
-  uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_bar, total;
+  uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_rms, off_bar, total;
 };
 
 __host__ __device__ inline SmemLayout score_smem_layout(int item_n) {
@@ -55,7 +57,8 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n) {
   L.off_b = kStages * L.a_bytes;
   L.off_w2 = L.off_b + kStages * L.b_bytes;
   L.off_b1 = L.off_w2 + kMaxDg * 4;
-  L.off_bar = L.off_b1 + kMaxDg * 4;
+  L.off_rms = L.off_b1 + kMaxDg * 4;           // [2 tiles][128 rows] fp32 1 / rms
+  L.off_bar = L.off_rms + 2 * kBM * 4;
   L.total = L.off_bar + 256 + 1024;  // barriers + slots, plus alignment slack
   return L;
 }
@@ -87,7 +90,8 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool NORM>
+__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -103,7 +107,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t *acc_full = empty + kStages;  // [2] MMA -> epilogue
   uint64_t *acc_empty = acc_full + 2;    // [2] epilogue -> MMA
   uint64_t *drain = acc_empty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *rms_ready = drain + 1;       // [2] norm warps -> epilogue (by tile parity)
+  uint64_t *rms_free = rms_ready + 2;    // [2] epilogue -> norm warps
+  float *s_inv_rms = reinterpret_cast<float *>(smem + L.off_rms);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rms_free + 2);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
   int32_t *n_consumed = abort_flag + 2;
@@ -114,13 +121,18 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       tg::mbar_init(&full[i], 1);
-      tg::mbar_init(&empty[i], kPair);  // one MMA commit from each CTA of the pair
+      // one MMA commit from each CTA of the pair (+ this CTA's four norm warps)
+      tg::mbar_init(&empty[i], kPair + (NORM ? 4 : 0));
     }
     for (int i = 0; i < 2; ++i) {
       tg::mbar_init(&acc_full[i], 1);
       tg::mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
     }
     tg::mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      tg::mbar_init(&rms_ready[i], 4);
+      tg::mbar_init(&rms_free[i], 4);
+    }
     *abort_flag = 0;
     *n_issued = 0;
     *n_consumed = 0;
@@ -134,7 +146,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tg::pdl_wait();
   tg::pdl_launch_dependents();
-  for (int i = threadIdx.x; i < p.d_g; i += kThreads) {
+  for (int i = threadIdx.x; i < p.d_g; i += blockDim.x) {
     s_w2[i] = tg::bf16_bits_to_float(p.w2[i]);
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
@@ -222,16 +234,22 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ---- epilogue: one row per thread; SiLU . w2 over each slice, sigmoid at the end ----
     const int quarter = warp & 3;  // tensor-memory lane quarter this warp may read
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    int it = 0;
+    int it = 0, ti = 0;
     bool ok = true;
-    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
+    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride, ++ti) {
       const int tile = pr * kPair + static_cast<int>(rank);
       float acc = 0.0f;
+      float inv_rms = 1.0f;
+      if (NORM) {
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&rms_ready[ti & 1], (ti >> 1) & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        inv_rms = s_inv_rms[(ti & 1) * kBM + r];
+      }
       for (int item = 0; item < p.n_items; ++item, ++it) {
         const int buf = it & 1;
         // tcgen05.ld is warp-collective: the whole warp takes the same branch
@@ -246,7 +264,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
           tg::tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float u = __uint_as_float(v[i]) + s_b1[hid0 + c0 + i];
+            const float u = NORM ? fmaf(__uint_as_float(v[i]), inv_rms, s_b1[hid0 + c0 + i])
+                                 : __uint_as_float(v[i]) + s_b1[hid0 + c0 + i];
             const float silu = __fdividef(u, 1.0f + __expf(-u));
             acc = fmaf(s_w2[hid0 + c0 + i], silu, acc);
           }
@@ -256,6 +275,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) tg::mbar_arrive(&acc_empty[buf]);
       }
       if (!ok) break;
+      if (NORM) {
+        __syncwarp();
+        if (lane == 0) tg::mbar_arrive(&rms_free[ti & 1]);  // this tile's 1/rms slots are free
+      }
       const int row = tile * kBM + r;
       if (row < p.T) {
         const float s = acc + p.b2;
@@ -263,6 +286,47 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         if (p.g_out) {
           const bool keep_always = p.mask && p.mask[row];
           p.g_out[row] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
+        }
+      }
+    }
+    if (!ok) *vabort = 1;
+  } else if (NORM) {
+    // ---- norm warps: sum of squares of each row of the tile as its h stages stream past ----
+    // Row r of a 128-byte-swizzled stage holds its eight 16-byte chunks at positions c ^ (r % 8).
+    const int r = (warp - 6) * 32 + lane;
+    int kc = 0, ti = 0;
+    bool ok = true;
+    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride, ++ti) {
+      float sq = 0.0f;
+      for (int item = 0; item < p.n_items && ok; ++item) {
+        for (int kt = 0; kt < p.KT; ++kt, ++kc) {
+          const int st = kc % kStages;
+          ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&full[st], (kc / kStages) & 1, vabort, p.wait_limit));
+          if (!ok) break;
+          if (item == 0) {  // every slice re-reads the same h tile; the first pass suffices
+            const uint4 *row_base = reinterpret_cast<const uint4 *>(sA + st * L.a_bytes + r * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 q = row_base[c ^ (r & 7)];
+              const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+                sq = fmaf(lo, lo, sq);
+                sq = fmaf(hi, hi, sq);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) tg::mbar_arrive(&empty[st]);
+        }
+        if (ok && item == 0) {
+          ok = __all_sync(0xFFFFFFFFu,
+                          tg::mbar_wait(&rms_free[ti & 1], ((ti >> 1) & 1) ^ 1u, vabort, p.wait_limit));
+          if (!ok) break;
+          s_inv_rms[(ti & 1) * kBM + r] = 1.0f / sqrtf(sq / static_cast<float>(p.d) + p.ln_eps);
+          __syncwarp();
+          if (lane == 0) tg::mbar_arrive(&rms_ready[ti & 1]);
         }
       }
     }
@@ -296,12 +360,13 @@ namespace tg_host {
 tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8_t *mask,
                             const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
                             int32_t d_g, float *s_out, float *g_out, int32_t *status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool rmsnorm, float ln_eps) {
   if (T == 0) return TG_OK;
   ScoreParams p;
   p.T = T;
   p.d = d;
   p.d_g = d_g;
+  p.ln_eps = ln_eps;
   p.n_items = d_g > kMaxItemN ? 2 : 1;
   p.item_n = d_g / p.n_items;  // d_g % 32 == 0, so a multiple of 16, at most 256
   p.n_tiles = (T + kBM - 1) / kBM;
@@ -333,14 +398,39 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
       return TG_ERR_CUDA;
   }
   const SmemLayout L = score_smem_layout(p.item_n);
-  cudaError_t e = cudaFuncSetAttribute(gate_score_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (e != cudaSuccess) return record_cuda(e);
   const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
   int pairs = num_sms() / kPair;
   if (pairs > n_pairs) pairs = n_pairs;
-  return record_cuda(launch_pdl(gate_score_kernel, dim3(pairs * kPair), dim3(kThreads), L.total,
-                                stream, tm_h, tm_w, p));
+  auto kernel = rmsnorm ? gate_score_kernel<true> : gate_score_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (e != cudaSuccess) return record_cuda(e);
+  return record_cuda(launch_pdl(kernel, dim3(pairs * kPair), dim3(rmsnorm ? kThreadsNorm : kThreads),
+                                L.total, stream, tm_h, tm_w, p));
+}
+
+// ---------------------------------------------------------------------------
+// W1' = W1 diag(w_ln): folds the RMSNorm weight into the first score layer, so the fused
+// kernel only has to scale each row's accumulator by its 1 / rms.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) fold_rmsnorm_weight_kernel(const uint16_t *W1, const uint16_t *ln_w,
+                                                                  int32_t d_g, int32_t d, uint16_t *W1_out) {
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
+  const long long n = static_cast<long long>(d_g) * d;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += static_cast<long long>(gridDim.x) * 256) {
+    const int c = static_cast<int>(i % d);
+    W1_out[i] = tg::float_to_bf16_bits(tg::bf16_bits_to_float(W1[i]) * tg::bf16_bits_to_float(ln_w[c]));
+  }
+}
+
+tg_status launch_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_w, int32_t d_g, int32_t d,
+                                     uint16_t *W1_out, cudaStream_t stream) {
+  const long long n = static_cast<long long>(d_g) * d;
+  long long grid = (n + 255) / 256;
+  if (grid > num_sms() * 8) grid = num_sms() * 8;
+  return record_cuda(launch_pdl(fold_rmsnorm_weight_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, stream,
+                                W1, ln_w, d_g, d, W1_out));
 }
 
 }  // namespace tg_host

@@ -119,3 +119,11 @@ def test_eq8_attention_rejects_bad_arguments(lib):
     assert call(p, f(ones), f(neg)) == binding.TG_ERR_INVALID_ARG              # temperature >= 0
     assert call(p, f(ones), f(ones), dh=96) == binding.TG_ERR_UNSUPPORTED
     assert call(p, f(ones), f(ones), hq=12, hkv=8) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_rmsnorm_entry_points_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.tg_gate_score_rmsnorm(p, 10, 64, None, p, None, p, 0.0, 32, -1.0, p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_gate_score_rmsnorm(p, 10, 64, None, p, None, p, 0.0, 33, 1e-6, p, None, None, None) == binding.TG_ERR_UNSUPPORTED
+    assert lib.tg_fold_rmsnorm_weight(None, p, 4, 4, p, None) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_fold_rmsnorm_weight(p, p, 0, 4, p, None) == binding.TG_ERR_INVALID_ARG

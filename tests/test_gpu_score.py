@@ -64,3 +64,72 @@ def test_score_full_size_sweep_sampled_rows():
     rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(wl.T_total - 300, wl.T_total),
                                      rng.integers(0, wl.T_total, 2000)]))
     _score(wl, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# Fused LN_2 (RMSNorm) in front of the score MLP (deep dive section 2, Eq. (1))
+# ---------------------------------------------------------------------------
+
+def _rmsnorm_case(wl, rows=None, ln_eps=1e-6):
+    gi = I.make_gate_inputs(wl)
+    T, d = wl.T_total, wl.d
+    rng = np.random.default_rng(61)
+    # the raw residual: rows of very different scale, so 1/rms matters
+    scale = rng.uniform(0.2, 8.0, T).astype(np.float32)
+    h_bits = I.f32_to_bf16_bits(I.bf16_bits_to_f32(gi["h"]) * scale[:, None])
+    ln_bits = I.f32_to_bf16_bits(rng.uniform(0.5, 1.5, d).astype(np.float32))
+    W1_d = dev(gi["W1"])
+    W1f = torch.zeros_like(W1_d)
+    tg.fold_rmsnorm_weight(W1_d, dev(ln_bits), W1f)
+    torch.cuda.synchronize()
+    # folding is a bf16 product rounded to nearest even
+    want_fold = I.f32_to_bf16_bits(I.bf16_bits_to_f32(gi["W1"]) * I.bf16_bits_to_f32(ln_bits)[None, :])
+    assert np.array_equal(host(W1f), want_fold)
+    s = torch.full((T + 32,), 12345.0, dtype=torch.float32, device="cuda")
+    g = torch.full((T + 32,), 12345.0, dtype=torch.float32, device="cuda")
+    st = status_word()
+    tg.gate_score_rmsnorm(dev(h_bits), W1f, dev(gi["w2"]), s[:T], g[:T], instr_mask=dev(gi["instr_mask"]),
+                          ln_eps=ln_eps, status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    s_h, g_h = host(s), host(g)
+    assert np.all(s_h[T:] == 12345.0) and np.all(g_h[T:] == 12345.0)
+    sel = slice(None) if rows is None else rows
+    ref_s, ref_g = O.gate_score(I.bf16_bits_to_f64(h_bits[sel]), I.bf16_bits_to_f64(gi["W1"]),
+                                I.bf16_bits_to_f64(gi["w2"]), gi["instr_mask"][sel],
+                                ln_weight=I.bf16_bits_to_f64(ln_bits), ln_eps=ln_eps)
+    # The folded weight adds one bf16 rounding (round to nearest: relative error uniform in
+    # +-2^-9, independent per entry) to every W1 diag(w_ln) entry. To first order it moves s by
+    # sum_k w2_k SiLU'(u_k) sum_c e_kc W1w_kc x_c, x = h / rms; with |SiLU'| <= 1.1 its standard
+    # deviation is at most sigma = 1.1 * 2^-9 / sqrt(3) * sqrt(sum_k w2_k^2 sum_c (W1w_kc x_c)^2).
+    # Allowed: 6 sigma on top of the plain score tolerance (fp32 accumulation).
+    h64 = I.bf16_bits_to_f64(h_bits[sel])
+    x = h64 / np.sqrt(np.mean(h64 * h64, axis=1, keepdims=True) + ln_eps)
+    W1w = I.bf16_bits_to_f64(gi["W1"]) * I.bf16_bits_to_f64(ln_bits)[None, :]
+    var = (I.bf16_bits_to_f64(gi["w2"]) ** 2) @ ((W1w ** 2) @ (x ** 2).T)        # [rows]
+    sigma = 1.1 * 2.0 ** -9 / np.sqrt(3.0) * np.sqrt(var)
+    err = np.abs(s_h[:T][sel] - ref_s)
+    assert np.all(err <= 6.0 * sigma + S_ATOL + S_RTOL * np.abs(ref_s)), float(np.max(err / (6.0 * sigma + S_ATOL)))
+    assert float(np.mean(err)) < 2.0 * float(np.mean(sigma)) + S_ATOL          # and typical errors are ~sigma
+    np.testing.assert_allclose(g_h[:T][sel], ref_g, rtol=0, atol=G_ATOL)
+
+
+def test_score_rmsnorm_tiny():
+    _rmsnorm_case(I.WORKLOADS["tiny"])
+
+
+def test_score_rmsnorm_ragged_tail_two_slices():
+    _rmsnorm_case(I.with_changes(I.WORKLOADS["tiny"], doc_lens=(900,), instr_lens=(17,), d=512, d_g=384),
+                  ln_eps=1e-5)
+
+
+def test_score_rmsnorm_qwen3_gate_layer_8k():
+    _rmsnorm_case(I.WORKLOADS["qwen3_1p7b_8k"])
+
+
+def test_score_rmsnorm_full_size_sweep_sampled_rows():
+    wl = I.WORKLOADS["sweep_32k"]
+    rng = np.random.default_rng(62)
+    rows = np.unique(np.concatenate([np.arange(0, 200), np.arange(wl.T_total - 200, wl.T_total),
+                                     rng.integers(0, wl.T_total, 1500)]))
+    _rmsnorm_case(wl, rows=rows)
