@@ -535,6 +535,58 @@ def paper_form(path, torch, flush, steps):
             "note": "single launches with events around each (launch gap included), L2 flushed before each"}
 
 
+def two_budget(path, torch, flush, steps):
+    """The packed two-budget forward (Eq. (9)) on the bench batch: one scoring pass, the full
+    and the pruned keep lists packed as 2B sequences, then ONE attention call over the pack;
+    against the same two budgets run as separate prune + attention calls."""
+    from learned_token_pruning_07_b300 import binding as tg
+    wl, T, B, d = path.wl, path.wl.T_total, path.wl.B, path.d
+    e = lambda *shape, dt=torch.float32: torch.empty(*shape, dtype=dt, device="cuda")
+    kept, cu = e(2 * T, dt=torch.int32), e(2 * B + 1, dt=torch.int32)
+    h_kept, pos_kept, g_kept = e(2 * T, wl.d, dt=torch.int16), e(2 * T, dt=torch.int32), e(2 * T)
+    M = T + path.M
+    gen = torch.Generator(device="cuda").manual_seed(wl.seed + 9)
+    Q = torch.randn((M, wl.H_q, wl.d_h), generator=gen, device="cuda").to(torch.bfloat16)
+    Kt = torch.randn((M, wl.H_kv, wl.d_h), generator=gen, device="cuda").to(torch.bfloat16)
+    V = torch.randn((M, wl.H_kv, wl.d_h), generator=gen, device="cuda").to(torch.bfloat16)
+    O = torch.empty_like(Q)
+    max_len = max(wl.seq_lens)
+
+    def packed():
+        tg.two_budget_prune_layer(d["h"], d["cu"], path.W1, path.w2, path.K, path.s, path.g, kept, cu, h_kept,
+                                  pos_kept=pos_kept, g_kept=g_kept, pos=d["pos"], instr_mask=d["mask"],
+                                  status=path.status)
+        tg.gated_attention(Q, Kt, V, cu, path.tau, path.beta, O, max_seqlen=max_len, g=g_kept, status=path.status)
+
+    def separate():
+        path.step()   # the pruned budget: score, select, gather, attention
+        tg.gated_attention(Q[:T], Kt[:T], V[:T], d["cu"], path.tau, path.beta, O[:T], max_seqlen=max_len,
+                           g=path.g, status=path.status)  # the full budget's attention
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, min(steps, 10))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    p_ms, s_ms = timed(packed), timed(separate)
+    assert tg.read_device_status(path.status) == 0, "device reported an error"
+    del Q, Kt, V, O, h_kept
+    torch.cuda.empty_cache()
+    return {"K_full": "all document tokens", "K_prune": path.K, "packed_rows": M,
+            "packed_ms": p_ms, "separate_ms": s_ms,
+            "note": "one scoring pass + one attention call over the 2B-sequence pack, vs the pruned step plus "
+                    "a separate full-budget attention call; host launches inside the events"}
+
+
 def workload_label(wl, K):
     docs = wl.doc_lens if wl.B > 1 else wl.doc_lens[0]
     ins = wl.instr_lens if wl.B > 1 else wl.instr_lens[0]
@@ -671,6 +723,7 @@ def run_gpu(args, rank, world, local):
                 torch.cuda.empty_cache()
 
     paper = paper_form(path, torch, flush, args.steps) if rank == 0 else None
+    twob = two_budget(path, torch, flush, args.steps) if rank == 0 else None
     longctx = long_context(torch, flush, args.steps) if (args.long_context and rank == 0) else None
 
     cpu = None
@@ -704,6 +757,8 @@ def run_gpu(args, rank, world, local):
             line["sweep"] = sweep
         if paper:
             line["paper_form"] = paper
+        if twob:
+            line["two_budget"] = twob
         if longctx:
             line["long_context"] = longctx
         print(json.dumps(line), flush=True)

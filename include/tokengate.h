@@ -192,6 +192,26 @@ TG_API tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, cons
                               int32_t *status, tg_stream_t stream);
 
 /*
+ * tg_two_budget_prune_layer — the packed two-budget forward of training (deep dive section 3.3,
+ *   Eq. (9): K_full = |P| and K_prune ~ LogUniform(1, |P|/2), "packed into one variable-length
+ *   call", phase 1 evaluated once). Scores once, then writes ONE keep list of 2B sequences:
+ *   sequences 0..B-1 are the full budget (every row: the identity) and sequences B..2B-1 the
+ *   K_prune selection of the same inputs, placed after them. cu_packed [device] int32 [2B+1]:
+ *   cu_packed[0..B] = cu_seqlens, cu_packed[B + b + 1] = T_total + (rows kept in the pruned
+ *   sequences 0..b). kept_idx / h_kept / pos_kept / g_kept follow the packed list, so one
+ *   tg_gated_attention call over (cu_packed, 2B sequences) serves both budgets.
+ *   capacity >= T_total is required; 2 * T_total is always enough. The caller draws K_prune.
+ *   Other arguments and errors as tg_gate_prune_layer; 1 <= B <= 512.
+ */
+TG_API tg_status tg_two_budget_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                                    const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                                    const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                                    int32_t d_g, int32_t K_prune, float *s_out, float *g_out,
+                                    int32_t *kept_idx, int32_t capacity, int32_t *cu_packed,
+                                    uint16_t *h_kept, int32_t *pos_kept, float *g_kept,
+                                    int32_t *status, tg_stream_t stream);
+
+/*
  * tg_apply_rope — rotate Q or K rows in place at their original position ids (rotate-half
  *   form, inv_freq_i = theta^(-2i/d_h)); the deep dive (section 3.4) keeps the original
  *   position ids for the kept tokens.

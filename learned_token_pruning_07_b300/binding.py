@@ -35,6 +35,8 @@ SIGNATURES = {
     "tg_gated_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tg_gate_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
                                  _P, _P, _P, _P, _P, _P]),
+    "tg_two_budget_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
+                                       _P, _P, _P, _P, _P, _P]),
     "tg_apply_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "tg_normalize_scores": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P]),
     "tg_gated_attention_eq8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -190,6 +192,19 @@ def gate_prune_layer(h, cu_seqlens, W1, w2, K: int, s_out, g_out, kept_idx, cu_k
                                     _ptr(cu_kept), _ptr(h_kept), _ptr(pos_kept), _ptr(g_kept),
                                     _ptr(status), _stream(stream))
     _check("tg_gate_prune_layer", st)
+
+
+def two_budget_prune_layer(h, cu_seqlens, W1, w2, K_prune: int, s_out, g_out, kept_idx, cu_packed, h_kept,
+                           pos_kept=None, g_kept=None, pos=None, instr_mask=None, b1=None, b2: float = 0.0,
+                           status=None, stream=None):
+    T, d = h.shape
+    B = cu_seqlens.numel() - 1
+    st = load().tg_two_budget_prune_layer(_ptr(h), _ptr(pos), _ptr(instr_mask), _ptr(cu_seqlens), B, T, d,
+                                          _ptr(W1), _ptr(b1), _ptr(w2), float(b2), W1.shape[0], int(K_prune),
+                                          _ptr(s_out), _ptr(g_out), _ptr(kept_idx), kept_idx.numel(),
+                                          _ptr(cu_packed), _ptr(h_kept), _ptr(pos_kept), _ptr(g_kept),
+                                          _ptr(status), _stream(stream))
+    _check("tg_two_budget_prune_layer", st)
 
 
 def apply_rope(X, pos, theta: float, cu_kept=None, stream=None):

@@ -13,12 +13,14 @@ tg_status launch_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_w, i
                                      uint16_t *W1_out, cudaStream_t stream);
 tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
                              int32_t B, int32_t T, int32_t K, int32_t *kept_idx, int32_t capacity,
-                             int32_t *cu_kept, int32_t *status, cudaStream_t stream);
+                             int32_t *cu_kept, int32_t *status, cudaStream_t stream, int32_t cu_base = 0);
 tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
                         const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t d,
                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int32_t B_kept = -1);
+tg_status launch_two_budget_prologue(const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t *kept_idx,
+                                     int32_t *cu_packed, cudaStream_t stream);
 tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
                       int32_t capacity, int32_t H, int32_t d_h, float theta, cudaStream_t stream);
 tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
@@ -190,6 +192,33 @@ tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8
   if (st != TG_OK) return st;
   return tg_host::launch_gather(h, pos, g_out, cu_seqlens, B, T_total, d, kept_idx, cu_kept,
                                 capacity, h_kept, pos_kept, g_kept, status, S(stream));
+}
+
+tg_status tg_two_budget_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                                    const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                                    const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
+                                    int32_t d_g, int32_t K_prune, float *s_out, float *g_out,
+                                    int32_t *kept_idx, int32_t capacity, int32_t *cu_packed,
+                                    uint16_t *h_kept, int32_t *pos_kept, float *g_kept,
+                                    int32_t *status, tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1, w2, d_g, s_out, b2);
+  if (st == TG_OK && !g_out) st = TG_ERR_INVALID_ARG;
+  if (st == TG_OK && capacity < T_total) st = TG_ERR_INVALID_ARG;  // the full half alone is T_total rows
+  if (st == TG_OK) st = check_select(s_out, cu_seqlens, B, T_total, K_prune, kept_idx, capacity, cu_packed);
+  if (st == TG_OK)
+    st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_packed, capacity, h_kept);
+  if (st == TG_OK && B > kMaxSelectB / 2) st = TG_ERR_UNSUPPORTED;
+  if (st != TG_OK) return st;
+  st = tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, w2, b2, d_g, s_out, g_out,
+                                  status, S(stream), false, 0.0f);
+  if (st != TG_OK) return st;
+  st = tg_host::launch_two_budget_prologue(cu_seqlens, B, T_total, kept_idx, cu_packed, S(stream));
+  if (st != TG_OK) return st;
+  st = tg_host::launch_topk_select(s_out, instr_mask, cu_seqlens, B, T_total, K_prune, kept_idx + T_total,
+                                   capacity - T_total, cu_packed + B, status, S(stream), T_total);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gather(h, pos, g_out, cu_seqlens, B, T_total, d, kept_idx, cu_packed, capacity,
+                                h_kept, pos_kept, g_kept, status, S(stream), 2 * B);
 }
 
 tg_status tg_apply_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,

@@ -19,6 +19,7 @@ struct GatherParams {
   const float *g;
   const int32_t *cu_seqlens;
   int32_t B, T, d;
+  int32_t B_kept;  // cu_kept has B_kept + 1 entries (B for one list; 2B for a two-budget pack)
   const int32_t *kept_idx;
   const int32_t *cu_kept;
   int32_t capacity;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
   // the first row's index is fetched together with the kept count (both sit in L2 from the
   // selection); an index at m >= M is read from inside the buffer but never used
   int j_next = m0 < p.capacity ? p.kept_idx[m0] : -1;
-  int M = min(p.cu_kept[p.B], p.capacity);
+  int M = min(p.cu_kept[p.B_kept], p.capacity);
   if (M < 0) M = 0;
   for (int m = m0; m < M; m += stride) {
     const int j = j_next;
@@ -90,6 +91,21 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
       if (p.g_kept && p.g) p.g_kept[m] = p.g[j];
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Two-budget packing: the full budget keeps every row, so its half of the packed keep list is
+// the identity and its boundaries are the input's.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) two_budget_prologue_kernel(const int32_t *cu_seqlens, int32_t B,
+                                                                   int32_t T, int32_t *kept_idx,
+                                                                   int32_t *cu_packed) {
+  tg::pdl_wait();
+  tg::pdl_launch_dependents();
+  const int stride = gridDim.x * 256;
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < T; i += stride) kept_idx[i] = i;
+  for (int i = blockIdx.x * 256 + threadIdx.x; i <= B; i += stride) cu_packed[i] = cu_seqlens[i];
 }
 
 // ---------------------------------------------------------------------------
@@ -143,15 +159,24 @@ tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
                         const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t d,
                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int32_t B_kept) {
   if (capacity == 0) return TG_OK;
-  GatherParams p{h, pos, g, cu_seqlens, B, T, d, kept_idx, cu_kept, capacity,
+  GatherParams p{h, pos, g, cu_seqlens, B, T, d, B_kept < 0 ? B : B_kept, kept_idx, cu_kept, capacity,
                  h_kept, pos_kept, g_kept, status};
   const int rows_per_wave = num_sms() * 8 * kGatherWarps;
   int grid = (capacity + kGatherWarps - 1) / kGatherWarps;
   if (grid > num_sms() * 8) grid = num_sms() * 8;
   (void)rows_per_wave;
   return record_cuda(launch_pdl(gather_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, p));
+}
+
+tg_status launch_two_budget_prologue(const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t *kept_idx,
+                                     int32_t *cu_packed, cudaStream_t stream) {
+  int grid = (T + 255) / 256;
+  if (grid < 1) grid = 1;
+  if (grid > num_sms() * 4) grid = num_sms() * 4;
+  return record_cuda(launch_pdl(two_budget_prologue_kernel, dim3(grid), dim3(256), 0, stream, cu_seqlens, B, T,
+                                kept_idx, cu_packed));
 }
 
 tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,

@@ -42,6 +42,7 @@ struct SelectParams {
   const uint8_t *mask;
   const int32_t *cu_seqlens;
   int32_t B, T, K, capacity, smem_keys;
+  int32_t cu_base;  // added to every cu_kept value (a list packed after cu_base earlier rows)
   int32_t vec;  // s is 16-byte and mask 4-byte aligned: stage keys with vector loads
   int32_t *kept_idx;
   int32_t *cu_kept;
@@ -403,8 +404,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   // this CTA is done reading its peers' shared memory (the loads have returned)
   cluster_arrive_relaxed();
   if (rank == 0 && tid == 0) {
-    if (b == 0) p.cu_kept[0] = 0;
-    p.cu_kept[b + 1] = sh.m_b;
+    if (b == 0) p.cu_kept[0] = p.cu_base;
+    p.cu_kept[b + 1] = p.cu_base + sh.m_b;
   }
 
   // ---- ordered write of this warp's kept rows ----
@@ -441,7 +442,7 @@ namespace tg_host {
 
 tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
                              int32_t B, int32_t T, int32_t K, int32_t *kept_idx, int32_t capacity,
-                             int32_t *cu_kept, int32_t *status, cudaStream_t stream) {
+                             int32_t *cu_kept, int32_t *status, cudaStream_t stream, int32_t cu_base) {
   SelectParams p;
   p.s = s;
   p.mask = mask;
@@ -453,6 +454,7 @@ tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t 
   p.kept_idx = kept_idx;
   p.cu_kept = cu_kept;
   p.status = status;
+  p.cu_base = cu_base;
   // every sequence is at most T long, so its chunk is at most ceil(T / kCluster) keys
   int keys = (T + kCluster - 1) / kCluster;
   keys = keys < 1 ? 1 : (keys > kMaxSmemKeys ? kMaxSmemKeys : keys);

@@ -319,3 +319,16 @@ def gate_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K, b1=None, b2=0.0)
     h_k, p_k, g_k = gather_kept(h, pos, g, kept_idx, cu_seqlens)
     return {"s": s, "g": g, "kept_idx": kept_idx, "cu_kept": cu_kept,
             "h_kept": h_k, "pos_kept": p_k, "g_kept": g_k}
+
+
+def two_budget_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K_prune, b1=None, b2=0.0):
+    """The packed two-budget forward (deep dive section 3.3, Eq. (9)): K_full = |P| keeps every
+    row, K_prune keeps the pruned set; both lists over the same scores (phase 1 evaluated
+    once), packed as 2B sequences: the B full ones first, then the B pruned ones."""
+    full = gate_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, len(instr_mask), b1, b2)
+    prune = gate_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K_prune, b1, b2)
+    T = len(instr_mask)
+    cu = np.concatenate([full["cu_kept"], T + prune["cu_kept"][1:]]).astype(np.int32)
+    cat = lambda k: np.concatenate([full[k], prune[k]])
+    return {"s": full["s"], "g": full["g"], "kept_idx": cat("kept_idx"), "cu_packed": cu,
+            "h_kept": cat("h_kept"), "pos_kept": cat("pos_kept"), "g_kept": cat("g_kept")}

@@ -11,7 +11,7 @@ import torch
 from learned_token_pruning_07_b300 import binding as tg
 from learned_token_pruning_07_b300 import inputs as I
 from oracle import tokengate_oracle as O
-from tests._helpers import (ATTN_MAX_ABS, ATTN_MEAN_REL, G_ATOL, S_ATOL, S_RTOL, attention_close,
+from tests._helpers import (ATTN_MAX_ABS, ATTN_MEAN_REL, G_ATOL, S_ATOL, S_RTOL, attention_close, sampled_rows,
                             bf16_dev_to_f64, dev, host, status_word, zeros_i32)
 
 pytestmark = pytest.mark.gpu
@@ -120,3 +120,74 @@ def test_rope_matches_oracle():
     # one bf16 rounding of values of magnitude up to ~5: half an ulp is 2^-8 * 4 / 2
     np.testing.assert_allclose(got, want, rtol=0, atol=2e-2)
     assert np.mean(np.abs(got - want)) < 2e-3
+
+
+# ---------------------------------------------------------------------------
+# The packed two-budget forward (deep dive section 3.3, Eq. (9))
+# ---------------------------------------------------------------------------
+
+def _two_budget(wl, K_prune):
+    gi = I.make_gate_inputs(wl)
+    T, B = wl.T_total, wl.B
+    t = {"s": torch.zeros(T, dtype=torch.float32, device="cuda"),
+         "g": torch.zeros(T, dtype=torch.float32, device="cuda"),
+         "kept": torch.full((2 * T,), -7, dtype=torch.int32, device="cuda"),
+         "cu": torch.full((2 * B + 1,), -7, dtype=torch.int32, device="cuda"),
+         "h_kept": torch.zeros((2 * T, wl.d), dtype=torch.int16, device="cuda"),
+         "pos_kept": zeros_i32(2 * T), "g_kept": torch.zeros(2 * T, dtype=torch.float32, device="cuda"),
+         "st": status_word()}
+    tg.two_budget_prune_layer(dev(gi["h"]), dev(gi["cu_seqlens"]), dev(gi["W1"]), dev(gi["w2"]), K_prune, t["s"],
+                              t["g"], t["kept"], t["cu"], t["h_kept"], pos_kept=t["pos_kept"], g_kept=t["g_kept"],
+                              pos=dev(gi["pos"]), instr_mask=dev(gi["instr_mask"]), status=t["st"])
+    torch.cuda.synchronize()
+    assert int(host(t["st"])[0]) == 0
+    out = {k: host(v) for k, v in t.items()}
+    ref = O.two_budget_prune_layer(I.bf16_bits_to_f64(gi["h"]), gi["pos"], I.bf16_bits_to_f64(gi["W1"]),
+                                   I.bf16_bits_to_f64(gi["w2"]), gi["instr_mask"], gi["cu_seqlens"], K_prune)
+    assert out["cu"].tolist() == ref["cu_packed"].tolist()
+    M = int(ref["cu_packed"][-1])
+    assert out["kept"][:T].tolist() == list(range(T))
+    assert np.all(out["kept"][M:] == -7)                                  # nothing past the packed list
+    # the pruned half: the selection property on the GPU's own scores (near-ties may fall
+    # either way against the fp64 oracle, as in the single-budget test)
+    for b in range(B):
+        a, e = int(out["cu"][B + b]), int(out["cu"][B + b + 1])
+        seg = out["kept"][a:e]
+        assert np.all(np.diff(seg) > 0)
+        lo, hi = int(gi["cu_seqlens"][b]), int(gi["cu_seqlens"][b + 1])
+        mask = gi["instr_mask"]
+        assert {j for j in range(lo, hi) if mask[j]} <= set(seg.tolist())
+        kd = [j for j in seg if not mask[j]]
+        pd = [j for j in range(lo, hi) if not mask[j] and j not in set(seg.tolist())]
+        if kd and pd:
+            assert out["s"][kd].min() >= out["s"][pd].max()
+    kept = out["kept"][:M]
+    assert np.array_equal(out["h_kept"][:M], gi["h"][kept])
+    assert np.array_equal(out["pos_kept"][:M], gi["pos"][kept])
+    assert np.array_equal(out["g_kept"][:M], out["g"][kept])
+    return gi, out, ref
+
+
+def test_two_budget_prune_tiny():
+    _two_budget(I.WORKLOADS["tiny"], 37)
+
+
+def test_two_budget_prune_ragged_and_one_attention_call():
+    wl = I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], doc_lens=(700, 0, 1500), instr_lens=(40, 8, 64))
+    gi, out, ref = _two_budget(wl, 300)
+    cu = out["cu"]
+    M = int(cu[-1])
+    at = I.make_attention_inputs(wl, M)
+    O_d = torch.zeros((M, wl.H_q, wl.d_h), dtype=torch.int16, device="cuda")
+    st = status_word()
+    lens = np.diff(cu)
+    tg.gated_attention(dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(cu), at["tau"], at["beta"], O_d,
+                       max_seqlen=int(lens.max()), g=dev(out["g_kept"][:M]), status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    rows = sampled_rows(cu, [], 300, seed=13)
+    want = O.gated_attention(I.bf16_bits_to_f64(at["Q"]), I.bf16_bits_to_f64(at["K"]),
+                             I.bf16_bits_to_f64(at["V"]), out["g_kept"][:M].astype(np.float64), cu,
+                             at["tau"].astype(np.float64), at["beta"].astype(np.float64), rows=rows)
+    mx, mr = attention_close(bf16_dev_to_f64(O_d)[rows], want)
+    assert mx <= ATTN_MAX_ABS and mr <= ATTN_MEAN_REL, (mx, mr)

@@ -479,6 +479,32 @@ def test_planted_eq8_mistakes_fail_the_rowwise_pin(kind):
 
 
 # ---------------------------------------------------------------------------
+# The packed two-budget forward (Eq. (9))
+# ---------------------------------------------------------------------------
+
+def test_two_budget_pack_invariants():
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(50, 0, 33), instr_lens=(4, 2, 6), d=64, d_g=32)
+    gi = I.make_gate_inputs(wl)
+    h = I.bf16_bits_to_f64(gi["h"])
+    W1, w2 = I.bf16_bits_to_f64(gi["W1"]), I.bf16_bits_to_f64(gi["w2"])
+    T, B = wl.T_total, wl.B
+    out = O.two_budget_prune_layer(h, gi["pos"], W1, w2, gi["instr_mask"], gi["cu_seqlens"], 7)
+    cu = out["cu_packed"]
+    assert out["kept_idx"][:T].tolist() == list(range(T))            # K_full = |P| keeps every row
+    assert cu[:B + 1].tolist() == gi["cu_seqlens"].tolist() and cu[B] == T
+    for b in range(B):                                               # |S_b| = min(K, |P_b|) + |N_b|
+        assert cu[B + b + 1] - cu[B + b] == min(7, wl.doc_lens[b]) + wl.instr_lens[b]
+    assert np.array_equal(out["h_kept"], h[out["kept_idx"]])
+    # sequences are independent: attention over the packed batch = attention over each half
+    at = I.make_attention_inputs(wl, int(cu[-1]))
+    Q, K, V = (I.bf16_bits_to_f64(at[k]) for k in ("Q", "K", "V"))
+    whole = O.gated_attention(Q, K, V, out["g_kept"], cu, at["tau"], at["beta"])
+    M = int(cu[-1])
+    second = O.gated_attention(Q[T:], K[T:], V[T:], out["g_kept"][T:], cu[B:] - T, at["tau"], at["beta"])
+    np.testing.assert_allclose(whole[T:M], second, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
 # RoPE
 # ---------------------------------------------------------------------------
 
