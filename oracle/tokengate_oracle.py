@@ -332,3 +332,64 @@ def two_budget_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K_prune, b1=N
     cat = lambda k: np.concatenate([full[k], prune[k]])
     return {"s": full["s"], "g": full["g"], "kept_idx": cat("kept_idx"), "cu_packed": cu,
             "h_kept": cat("h_kept"), "pos_kept": cat("pos_kept"), "g_kept": cat("g_kept")}
+
+
+# ---------------------------------------------------------------------------
+# Backward of token-gated attention (deep dive section 3.2: the gate score reaches the loss
+# only through the attention bias; section 3.1: no gradient crosses the top-K choice itself).
+# ---------------------------------------------------------------------------
+
+def gated_attention_bwd(Q, K, V, g, dO, cu_kept, tau, beta):
+    """Gradients of L = sum(dO * o) for o = gated_attention(Q, K, V, g, cu_kept, tau, beta).
+
+    With x_ij = tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j over j <= i in the sequence,
+    P = softmax_j(x), o_i = sum_j P_ij v_j:
+      dV_j += P_ij dO_i;  dP_ij = dO_i.v_j;  D_i = dO_i.o_i;  dX_ij = P_ij (dP_ij - D_i);
+      dQ_i = tau_h / sqrt(d_h) sum_j dX_ij k_j;  dK_j += tau_h / sqrt(d_h) dX_ij q_i;
+      dbias[j, h] = sum_i dX_ij  (the gradient w.r.t. the head-h bias beta_h ln g_j).
+    Query heads of a GQA group add into their kv head's dK, dV. Returns float64
+    (dQ [M,H_q,d], dK [M,H_kv,d], dV [M,H_kv,d], dbias [M,H_q]).
+    """
+    Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    group = H_q // H_kv
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dbias = np.zeros((M, H_q))
+    cu = np.asarray(cu_kept, dtype=np.int64)
+    c = 1.0 / math.sqrt(d_h)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        if n == 0:
+            continue
+        causal = np.tril(np.ones((n, n), dtype=bool))
+        for h in range(H_q):
+            kv = h // group
+            q, k, v, do = Q[a:e, h], K[a:e, kv], V[a:e, kv], dO[a:e, h]
+            bias = _log_bias(None if g is None else np.asarray(g)[a:e], float(beta[h]), n)
+            x = np.where(causal, float(tau[h]) * c * (q @ k.T) + bias[None, :], -np.inf)
+            mx = x.max(axis=1, keepdims=True)
+            mx = np.where(np.isfinite(mx), mx, 0.0)
+            p = np.exp(x - mx)
+            l = p.sum(axis=1, keepdims=True)
+            P = np.where(l > 0, p / np.where(l > 0, l, 1.0), 0.0)
+            o = P @ v
+            dP = do @ v.T
+            D = np.sum(do * o, axis=1, keepdims=True)
+            dX = P * (dP - D)
+            dV[a:e, kv] += P.T @ do
+            dQ[a:e, h] = float(tau[h]) * c * (dX @ k)
+            dK[a:e, kv] += float(tau[h]) * c * (dX.T @ q)
+            dbias[a:e, h] = dX.sum(axis=0)
+    return dQ, dK, dV, dbias
+
+
+def gate_score_grad(dbias, beta, g_kept, kept_idx, T):
+    """dL/ds for every input row: the kept row j carries dL/d(ln g_j) = sum_h beta_h dbias[j, h]
+    and d ln g / ds = 1 - g for g = sigmoid(s); non-prunable rows have the constant g = 1 and
+    rows that were not kept get no gradient (the top-K choice itself has none)."""
+    dlng = np.asarray(dbias, dtype=np.float64) @ np.asarray(beta, dtype=np.float64)
+    ds = np.zeros(T)
+    ds[np.asarray(kept_idx, dtype=np.int64)] = dlng * (1.0 - np.asarray(g_kept, dtype=np.float64))
+    return ds

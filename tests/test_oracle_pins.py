@@ -505,6 +505,79 @@ def test_two_budget_pack_invariants():
 
 
 # ---------------------------------------------------------------------------
+# Backward of token-gated attention
+# ---------------------------------------------------------------------------
+
+def _torch_forward(Q, K, V, g, cu, tau, beta):
+    """The same forward written with torch CPU fp64 ops (causal softmax with the log-gate bias),
+    differentiable in Q, K, V and the per-head bias tensor."""
+    M, H_q, d_h = Q.shape
+    group = H_q // K.shape[1]
+    q, k, v = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (Q, K, V))
+    lng = torch.log(torch.tensor(g, dtype=torch.float64))
+    bias = (torch.tensor(beta, dtype=torch.float64)[None, :] * lng[:, None]).detach().requires_grad_(True)
+    outs = []
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        mask = torch.full((n, n), float("-inf"), dtype=torch.float64).triu(1)
+        heads = []
+        for h in range(H_q):
+            z = (q[a:e, h] @ k[a:e, h // group].T) * (float(tau[h]) / math.sqrt(d_h))
+            w = torch.softmax(z + bias[a:e, h][None, :] + mask, dim=1)
+            heads.append(w @ v[a:e, h // group])
+        outs.append(torch.stack(heads, dim=1))
+    return torch.cat(outs, dim=0), (q, k, v, bias)
+
+
+def test_attention_bwd_matches_torch_autograd():
+    Q, K, V, g, cu, tau, beta = _rand_attn(51, (9, 1, 14))
+    dO = np.random.default_rng(52).standard_normal(Q.shape)
+    dQ, dK, dV, dbias = O.gated_attention_bwd(Q, K, V, g, dO, cu, tau, beta)
+    out, (q, k, v, bias) = _torch_forward(Q, K, V, g, cu, tau, beta)
+    np.testing.assert_allclose(out.detach().numpy(), O.gated_attention(Q, K, V, g, cu, tau, beta),
+                               rtol=1e-12, atol=1e-12)
+    (out * torch.from_numpy(dO)).sum().backward()
+    for got, ref in ((dQ, q.grad), (dK, k.grad), (dV, v.grad), (dbias, bias.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_bwd_bias_gradient_by_finite_differences():
+    # d/d(ln g_j) of sum(dO * o) = sum_h beta_h dbias[j, h]: central differences on ln g
+    Q, K, V, g, cu, tau, beta = _rand_attn(53, (7, 5))
+    dO = np.random.default_rng(54).standard_normal(Q.shape)
+    _, _, _, dbias = O.gated_attention_bwd(Q, K, V, g, dO, cu, tau, beta)
+    loss = lambda gg: float(np.sum(dO * O.gated_attention(Q, K, V, gg, cu, tau, beta)))
+    eps = 1e-6
+    for j in (0, 3, 6, 7, 11):
+        up, dn = g.copy(), g.copy()
+        up[j] *= math.exp(eps)
+        dn[j] *= math.exp(-eps)
+        fd = (loss(up) - loss(dn)) / (2 * eps)
+        assert abs(fd - float(dbias[j] @ beta)) < 1e-6 * max(1.0, abs(fd))
+
+
+def test_gate_score_grad_chain():
+    # ds_j = (1 - g_j) * sum_h beta_h dbias[j, h] on kept rows, 0 elsewhere; by finite
+    # differences through g = sigmoid(s) on a kept document row
+    Q, K, V, _, cu, tau, beta = _rand_attn(55, (10,))
+    rng = np.random.default_rng(56)
+    s = rng.standard_normal(10)
+    g = 1.0 / (1.0 + np.exp(-s))
+    dO = rng.standard_normal(Q.shape)
+    _, _, _, dbias = O.gated_attention_bwd(Q, K, V, g, dO, cu, tau, beta)
+    kept = np.arange(10) * 2                                  # rows of a 20-row input
+    ds = O.gate_score_grad(dbias, beta, g, kept, 20)
+    assert np.all(ds[1::2] == 0.0)
+    loss = lambda ss: float(np.sum(dO * O.gated_attention(Q, K, V, 1.0 / (1.0 + np.exp(-ss)), cu, tau, beta)))
+    for j in (2, 5, 9):
+        up, dn = s.copy(), s.copy()
+        up[j] += 1e-6
+        dn[j] -= 1e-6
+        assert abs((loss(up) - loss(dn)) / 2e-6 - ds[kept[j]]) < 1e-6
+
+
+# ---------------------------------------------------------------------------
 # RoPE
 # ---------------------------------------------------------------------------
 
