@@ -385,6 +385,31 @@ def gated_attention_bwd(Q, K, V, g, dO, cu_kept, tau, beta):
     return dQ, dK, dV, dbias
 
 
+def gated_attention_lse(Q, K, g, cu_kept, tau, beta):
+    """ln sum_{j <= i} exp(x_ij) for every kept row i and query head h ([M, H_q]; -inf when
+    every key has zero weight), the normaliser the backward rebuilds P with."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    M, H_q, d_h = Q.shape
+    group = H_q // K.shape[1]
+    cu = np.asarray(cu_kept, dtype=np.int64)
+    out = np.full((M, H_q), -np.inf)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        if n == 0:
+            continue
+        causal = np.tril(np.ones((n, n), dtype=bool))
+        for h in range(H_q):
+            bias = _log_bias(None if g is None else np.asarray(g)[a:e], float(beta[h]), n)
+            x = np.where(causal, float(tau[h]) / math.sqrt(d_h) * (Q[a:e, h] @ K[a:e, h // group].T) + bias[None, :],
+                         -np.inf)
+            mx = x.max(axis=1)
+            fin = np.isfinite(mx)
+            out[a:e, h][fin] = mx[fin] + np.log(np.exp(x[fin] - mx[fin, None]).sum(axis=1))
+    return out
+
+
 def gate_score_grad(dbias, beta, g_kept, kept_idx, T):
     """dL/ds for every input row: the kept row j carries dL/d(ln g_j) = sum_h beta_h dbias[j, h]
     and d ln g / ds = 1 - g for g = sigmoid(s); non-prunable rows have the constant g = 1 and

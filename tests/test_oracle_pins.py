@@ -557,6 +557,18 @@ def test_attention_bwd_bias_gradient_by_finite_differences():
         assert abs(fd - float(dbias[j] @ beta)) < 1e-6 * max(1.0, abs(fd))
 
 
+def test_attention_lse_matches_torch_logsumexp():
+    Q, K, V, g, cu, tau, beta = _rand_attn(57, (6, 11))
+    got = O.gated_attention_lse(Q, K, g, cu, tau, beta)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        for h in range(Q.shape[1]):
+            z = torch.from_numpy(Q[a:e, h] @ K[a:e, h // 2].T) * (tau[h] / math.sqrt(Q.shape[2]))
+            z = z + beta[h] * torch.log(torch.from_numpy(g[a:e]))[None, :]
+            z = z.masked_fill(torch.ones(e - a, e - a, dtype=torch.bool).triu(1), float("-inf"))
+            np.testing.assert_allclose(got[a:e, h], torch.logsumexp(z, dim=1).numpy(), rtol=1e-12, atol=1e-12)
+
+
 def test_gate_score_grad_chain():
     # ds_j = (1 - g_j) * sum_h beta_h dbias[j, h] on kept rows, 0 elsewhere; by finite
     # differences through g = sigmoid(s) on a kept document row
