@@ -178,6 +178,51 @@ TG_API tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const 
                              int32_t *status, tg_stream_t stream);
 
 /*
+ * tg_gated_attention_lse — tg_gated_attention that also writes, for every kept row i and query
+ *   head h, lse[i * H_q + h] = ln sum_{j <= i} exp(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j)
+ *   (-inf when every key has zero weight): what the backward needs to rebuild P.
+ *   lse [device] fp32 [M_capacity, H_q]. Other arguments as tg_gated_attention.
+ */
+TG_API tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                 float *lse, int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_gated_attention_bwd — gradients of a loss through tg_gated_attention (deep dive section
+ *   3.2: the gate score reaches the loss only through the attention bias; section 3.1: the top-K
+ *   choice itself has no gradient). With P_ij = exp(x_ij - lse_i), dX_ij = P_ij (dO_i.v_j - dO_i.o_i):
+ *     dQ [device] fp32 [M, H_q, d_h]  = tau_h / sqrt(d_h) sum_j dX_ij k_j
+ *     dK, dV [device] fp32 [M, H_kv, d_h]: sums over the query heads of each GQA group
+ *     dbias [device] fp32 [M, H_q]: sum_i dX_ij, the gradient w.r.t. the head-h bias
+ *       beta_h ln g_j (so dL/d ln g_j = sum_h beta_h dbias[j, h]).
+ *   O, dO [device] bf16 [M, H_q, d_h] (the forward's output and the incoming gradient);
+ *   lse from tg_gated_attention_lse. Outputs are overwritten for rows < min(cu_kept[B], M_capacity).
+ *   Deterministic (fixed-order sums, no atomics). This version computes on the CUDA cores in
+ *   fp32 (64x64 tiles recomputed in shared memory). Other arguments as tg_gated_attention.
+ */
+TG_API tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const uint16_t *O, const uint16_t *dO,
+                                 const float *lse, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, float *dQ,
+                                 float *dK, float *dV, float *dbias, int32_t *status,
+                                 tg_stream_t stream);
+
+/*
+ * tg_gate_score_grad — carry the attention bias gradient back to the gate scores:
+ *   ds[kept_idx[m]] = (1 - g_kept[m]) * sum_h beta_h dbias[m, h] for m < min(cu_kept[B], capacity)
+ *   (d ln g / ds = 1 - g for g = sigmoid(s); non-prunable rows have g = 1, so they get 0).
+ *   Rows that were not kept are not written: the caller zeroes ds [device] fp32 [T_total].
+ *   dbias [device] fp32 [capacity, H_q]; beta [host] fp32 [H_q]; g_kept [device] fp32 [capacity].
+ */
+TG_API tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+                             const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
+                             int32_t capacity, int32_t H_q, int32_t T_total, float *ds,
+                             tg_stream_t stream);
+
+/*
  * tg_gate_prune_layer — tg_gate_score, tg_topk_select and tg_gather_kept enqueued back to
  *   back on one stream (the deep dive's section 3.4 prune path: score, clamp, select, keep
  *   indices, slice hidden states, gather positions). Arguments as in the three calls;

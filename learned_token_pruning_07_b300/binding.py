@@ -33,6 +33,10 @@ SIGNATURES = {
     "tg_topk_select": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "tg_gather_kept": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "tg_gated_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_gated_attention_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "tg_gated_attention_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                    _P, _P, _P]),
+    "tg_gate_score_grad": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "tg_gate_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
                                  _P, _P, _P, _P, _P, _P]),
     "tg_two_budget_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
@@ -179,6 +183,40 @@ def gated_attention_eq8(Q, K, V, cu_kept, pos, gain, temp, O, max_seqlen: int, b
                                        _stream(stream))
     del gain_a, temp_a
     _check("tg_gated_attention_eq8", st)
+
+
+def gated_attention_lse(Q, K, V, cu_kept, tau, beta, O, lse, max_seqlen: int, g=None, status=None, stream=None):
+    M, H_q, d_h = Q.shape
+    tau_a, tau_p = _host_f32(tau)
+    beta_a, beta_p = _host_f32(beta)
+    st = load().tg_gated_attention_lse(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(cu_kept), cu_kept.numel() - 1, M,
+                                       int(max_seqlen), H_q, K.shape[1], d_h, tau_p, beta_p, _ptr(O), _ptr(lse),
+                                       _ptr(status), _stream(stream))
+    del tau_a, beta_a
+    _check("tg_gated_attention_lse", st)
+
+
+def gated_attention_bwd(Q, K, V, O, dO, lse, cu_kept, tau, beta, dQ, dK, dV, dbias, max_seqlen: int, g=None,
+                        status=None, stream=None):
+    M, H_q, d_h = Q.shape
+    tau_a, tau_p = _host_f32(tau)
+    beta_a, beta_p = _host_f32(beta)
+    st = load().tg_gated_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(O), _ptr(dO), _ptr(lse),
+                                       _ptr(cu_kept), cu_kept.numel() - 1, M, int(max_seqlen), H_q, K.shape[1],
+                                       d_h, tau_p, beta_p, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbias),
+                                       _ptr(status), _stream(stream))
+    del tau_a, beta_a
+    _check("tg_gated_attention_bwd", st)
+
+
+def gate_score_grad(dbias, beta, g_kept, kept_idx, cu_kept, ds, stream=None):
+    H_q = dbias.shape[1]
+    beta_a, beta_p = _host_f32(beta)
+    st = load().tg_gate_score_grad(_ptr(dbias), beta_p, _ptr(g_kept), _ptr(kept_idx), _ptr(cu_kept),
+                                   cu_kept.numel() - 1, kept_idx.numel(), H_q, ds.numel(), _ptr(ds),
+                                   _stream(stream))
+    del beta_a
+    _check("tg_gate_score_grad", st)
 
 
 def gate_prune_layer(h, cu_seqlens, W1, w2, K: int, s_out, g_out, kept_idx, cu_kept, h_kept,

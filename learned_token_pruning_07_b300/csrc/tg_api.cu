@@ -27,7 +27,16 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
                                  const float *g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
-                                 int32_t *status, cudaStream_t stream);
+                                 int32_t *status, cudaStream_t stream, float *lse = nullptr);
+tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                     const float *g, const uint16_t *O, const uint16_t *dO,
+                                     const float *lse, const int32_t *cu_kept, int32_t B, int32_t M_cap,
+                                     int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h,
+                                     const float *tau, const float *beta, float *dQ, float *dK, float *dV,
+                                     float *dbias, int32_t *status, cudaStream_t stream);
+tg_status launch_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+                                 const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
+                                 int32_t capacity, int32_t H_q, int32_t T, float *ds, cudaStream_t stream);
 tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                                      const float *b, const int32_t *pos, const int32_t *cu_kept,
                                      int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q,
@@ -124,11 +133,10 @@ tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g,
                                 h_kept, pos_kept, g_kept, status, S(stream));
 }
 
-tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                             const float *g, const int32_t *cu_kept, int32_t B,
-                             int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
-                             int32_t d_h, const float *tau, const float *beta, uint16_t *O,
-                             int32_t *status, tg_stream_t stream) {
+namespace {
+tg_status check_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *cu_kept,
+                          int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                          int32_t d_h, const float *tau, const float *beta, const void *O) {
   if (!Q || !K || !V || !cu_kept || !tau || !beta || !O) return TG_ERR_INVALID_ARG;
   if (B < 1 || M_capacity < 0 || max_seqlen < 0 || H_q < 1 || H_kv < 1 || d_h < 1)
     return TG_ERR_INVALID_ARG;
@@ -138,8 +146,58 @@ tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_
     if (!std::isfinite(beta[h]) || beta[h] < 0.0f) return TG_ERR_INVALID_ARG;
   }
   if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+}  // namespace
+
+tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                             const float *g, const int32_t *cu_kept, int32_t B,
+                             int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                             int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                             int32_t *status, tg_stream_t stream) {
+  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  if (st != TG_OK) return st;
   return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
                                          d_h, tau, beta, O, status, S(stream));
+}
+
+tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                 float *lse, int32_t *status, tg_stream_t stream) {
+  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  if (st == TG_OK && !lse) st = TG_ERR_INVALID_ARG;
+  if (st != TG_OK) return st;
+  return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
+                                         d_h, tau, beta, O, status, S(stream), lse);
+}
+
+tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                 const float *g, const uint16_t *O, const uint16_t *dO,
+                                 const float *lse, const int32_t *cu_kept, int32_t B,
+                                 int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                 int32_t d_h, const float *tau, const float *beta, float *dQ,
+                                 float *dK, float *dV, float *dbias, int32_t *status,
+                                 tg_stream_t stream) {
+  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  if (st == TG_OK && (!dO || !lse || !dQ || !dK || !dV || !dbias)) st = TG_ERR_INVALID_ARG;
+  if (st != TG_OK) return st;
+  return tg_host::launch_gated_attention_bwd(Q, K, V, g, O, dO, lse, cu_kept, B, M_capacity, max_seqlen,
+                                             H_q, H_kv, d_h, tau, beta, dQ, dK, dV, dbias, status,
+                                             S(stream));
+}
+
+tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+                             const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
+                             int32_t capacity, int32_t H_q, int32_t T_total, float *ds,
+                             tg_stream_t stream) {
+  if (!dbias || !beta || !g_kept || !kept_idx || !cu_kept || !ds) return TG_ERR_INVALID_ARG;
+  if (B < 1 || capacity < 0 || H_q < 1 || H_q > 128 || T_total < 0) return TG_ERR_INVALID_ARG;
+  for (int h = 0; h < H_q; ++h)
+    if (!std::isfinite(beta[h])) return TG_ERR_INVALID_ARG;
+  return tg_host::launch_gate_score_grad(dbias, beta, g_kept, kept_idx, cu_kept, B, capacity, H_q, T_total, ds,
+                                         S(stream));
 }
 
 tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,

@@ -59,6 +59,7 @@ struct AttnParams {
   const int32_t *cu_kept;
   int32_t B, M_cap, max_seqlen, H_q, H_kv, group, heads_per_cta, pairs, n_qt_max;
   uint16_t *O;
+  float *lse;  // optional [M, H_q]: natural-log log-sum-exp of each row's logits (for the backward)
   int32_t *status;
   uint64_t wait_limit, drain_limit;
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
@@ -482,6 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
         const int row = q0 + r;
+        if (p.lse != nullptr && row < seq_len) {
+          // x is in log2 units relative to m_ref: ln sum exp = (m + log2 l) ln 2
+          const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+          p.lse[static_cast<size_t>(seq_start + row) * p.H_q + h] =
+              l > 0.0f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
         uint16_t *orow = p.O + (static_cast<size_t>(seq_start + row) * p.H_q + h) * D;
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -567,6 +574,7 @@ AttnParams common_params(const float *bias_src, const int32_t *pos, const int32_
                          int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv, uint16_t *O,
                          int32_t *status) {
   AttnParams p;
+  p.lse = nullptr;
   p.g = bias_src;
   p.pos = pos;
   p.cu_kept = cu_kept;
@@ -593,9 +601,10 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
                                  const float *g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
-                                 int32_t *status, cudaStream_t stream) {
+                                 int32_t *status, cudaStream_t stream, float *lse) {
   if (M_cap == 0 || max_seqlen == 0) return TG_OK;
   AttnParams p = common_params(g, nullptr, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
+  p.lse = lse;
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale_log2[h] = h < H_q ? tau[h] * log2e / std::sqrt(static_cast<float>(d_h)) : 0.0f;
