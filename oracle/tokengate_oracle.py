@@ -39,6 +39,12 @@ Readings for the exact gate form (normalize_scores, gated_attention_eq8): eps of
 the RMS normalisation is a parameter (default 1e-6; the pages give none); m_i is
 the number of retained keys query i sees (its index in the kept sequence + 1) and
 p_i the number of positions it originally saw (its original position + 1).
+
+Readings for per-head gate scores (the per-head bias and "uniform head aggregation for
+selection" of the deep dive's section 3.4): the score MLP's second layer has H_g rows, one
+score per gate head; selection ranks the row mean over heads, in fp32 as stored; query head h
+reads gate head floor(h / (H_q / H_g)), with H_g dividing H_q. In the exact form each head's
+scores are RMS-normalised on their own and selection ranks the mean of the normalised scores.
 """
 from __future__ import annotations
 
@@ -70,6 +76,9 @@ def gate_score(h: np.ndarray, W1: np.ndarray, w2: np.ndarray, instr_mask: np.nda
     Deep dive section 3.1, Eq. (3): b~_j = MLP(a~_j); the tokens in the
     non-prunable set carry no bias (read here as g_j = 1). With ln_weight given,
     h is the post-attention residual a^L and the MLP reads LN_2(a^L) (Eq. (1)).
+
+    Per-head scores (deep dive section 3.4: a per-head bias): w2 [H_g, d_g] and b2 a
+    scalar or [H_g] give one score per gate head, s and g [T, H_g].
     """
     if ln_weight is not None:
         h = rms_norm(h, ln_weight, ln_eps)
@@ -81,11 +90,36 @@ def gate_score(h: np.ndarray, W1: np.ndarray, w2: np.ndarray, instr_mask: np.nda
         u = u + np.asarray(b1, dtype=np.float64)[None, :]
     with np.errstate(over="ignore"):
         a = u / (1.0 + np.exp(-u))                 # SiLU(u) = u * sigmoid(u)
-    s = a @ w2 + float(b2)                         # [T]
+    if w2.ndim == 1:
+        s = a @ w2 + float(b2)                     # [T]
+    else:
+        s = a @ w2.T + np.asarray(b2, dtype=np.float64)   # [T, H_g]
     with np.errstate(over="ignore"):
         g = 1.0 / (1.0 + np.exp(-s))
-    g = np.where(np.asarray(instr_mask) != 0, 1.0, g)
+    keep = np.asarray(instr_mask) != 0
+    g = np.where(keep if g.ndim == 1 else keep[:, None], 1.0, g)
     return s, g
+
+
+def aggregate_heads(s: np.ndarray) -> np.ndarray:
+    """Uniform head aggregation for selection (deep dive section 3.4): the mean of a row's
+    per-head scores, s [T, H_g] -> [T]; a single-head score [T] is returned as it is."""
+    s = np.asarray(s, dtype=np.float64)
+    return s if s.ndim == 1 else s.mean(axis=1)
+
+
+def gate_column(h: int, H_q: int, H_g: int) -> int:
+    """The gate head that query head h reads: consecutive groups of H_q / H_g query heads
+    share one gate head (H_g = 1: every head reads the same gate)."""
+    return h // (H_q // H_g)
+
+
+def _head_gate(g: Optional[np.ndarray], h: int, H_q: int, a: int, e: int) -> Optional[np.ndarray]:
+    """Rows a..e-1 of the gate (or score bias) that query head h reads; None stays None."""
+    if g is None:
+        return None
+    g = np.asarray(g)
+    return g[a:e] if g.ndim == 1 else g[a:e, gate_column(h, H_q, g.shape[1])]
 
 
 # ---------------------------------------------------------------------------
@@ -162,8 +196,8 @@ def gated_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, g: Optional[np.
                     rows: Optional[Sequence[int]] = None) -> np.ndarray:
     """o_i = sum_{j<=i, same sequence} softmax_j(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j) v_j.
 
-    Q [M, H_q, d_h], K/V [M, H_kv, d_h], g [M] or None (no bias), cu_kept [B+1],
-    tau/beta [H_q]. ``rows`` restricts the output to those global query rows
+    Q [M, H_q, d_h], K/V [M, H_kv, d_h], g [M] or [M, H_g] (per-head gates, query head h
+    reads column gate_column(h)) or None (no bias), cu_kept [B+1], tau/beta [H_q]. ``rows`` restricts the output to those global query rows
     (each row is an independent softmax); the result is [len(rows), H_q, d_h]
     (or [M, H_q, d_h] when rows is None). Two passes per row: max, then the
     normalised sum.
@@ -190,7 +224,7 @@ def gated_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, g: Optional[np.
             end = int(r.max()) + 1
             keys = K[start:end, kv, :]
             vals = V[start:end, kv, :]
-            bias = _log_bias(None if g is None else g[start:end], float(beta[h]), end - start)
+            bias = _log_bias(_head_gate(g, h, H_q, start, end), float(beta[h]), end - start)
             z = (Q[r, h, :] @ keys.T) * inv_sqrt              # [rows, keys]
             logits = float(tau[h]) * z + bias[None, :]
             causal = (np.arange(start, end)[None, :] <= r[:, None])
@@ -233,8 +267,12 @@ def gated_attention_weights_eq5(Q: np.ndarray, K: np.ndarray, g: Optional[np.nda
 def normalize_scores(s: np.ndarray, instr_mask: np.ndarray, cu_seqlens: Sequence[int],
                      eps: float = 1e-6) -> np.ndarray:
     """Eq. (3): b_j = b~_j / sqrt(mean over the sequence's prunable rows of b~^2 + eps), and
-    b_j = 0 on the non-prunable rows. A sequence with no prunable row has b = 0 throughout."""
+    b_j = 0 on the non-prunable rows. A sequence with no prunable row has b = 0 throughout.
+    Per-head scores s [T, H_g] are normalised column by column."""
     s = np.asarray(s, dtype=np.float64)
+    if s.ndim == 2:  # per-head scores: each head is normalised over the sequence on its own
+        return np.stack([normalize_scores(s[:, c], instr_mask, cu_seqlens, eps) for c in range(s.shape[1])],
+                        axis=1)
     b = np.zeros_like(s)
     for i in range(len(cu_seqlens) - 1):
         a, e = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
@@ -261,7 +299,8 @@ def gated_attention_eq8(Q: np.ndarray, K: np.ndarray, V: np.ndarray, b: Optional
     gain_h = softplus(gamma_h) (>= 0), tau_i from Eq. (7) with temp_h = softplus(sigma_h).
     Query i of a sequence starting at kept row `start` sees m_i = i - start + 1 retained keys
     and originally saw p_i = pos_i + 1 positions (pos holds the original position ids).
-    b None means no score bias. Layouts and `rows` as in gated_attention; two passes per row.
+    b None means no score bias; b [M, H_g] holds per-head biases (query head h reads column
+    gate_column(h)). Layouts and `rows` as in gated_attention; two passes per row.
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -272,6 +311,8 @@ def gated_attention_eq8(Q: np.ndarray, K: np.ndarray, V: np.ndarray, b: Optional
     rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
     out = np.zeros((len(rows), H_q, d_h), dtype=np.float64)
     bias = np.zeros(M) if b is None else np.asarray(b, dtype=np.float64)
+    if bias.ndim == 1:
+        bias = bias[:, None]
     for n, i in enumerate(rows):
         seq = int(np.searchsorted(cu, i, side="right") - 1)
         start = int(cu[seq])
@@ -280,7 +321,7 @@ def gated_attention_eq8(Q: np.ndarray, K: np.ndarray, V: np.ndarray, b: Optional
             kv = h // group
             tau = query_temperature(temp[h], i - start + 1, int(pos[i]) + 1)
             z = (K[keys, kv, :] @ Q[i, h, :]) / math.sqrt(d_h)
-            logits = tau * (z + float(gain[h]) * bias[keys])
+            logits = tau * (z + float(gain[h]) * bias[keys, gate_column(h, H_q, bias.shape[1])])
             w = np.exp(logits - logits.max())
             out[n, h, :] = (w / w.sum()) @ V[keys, kv, :]
     return out
@@ -314,8 +355,9 @@ def apply_rope(X: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def gate_prune_layer(h, pos, W1, w2, instr_mask, cu_seqlens, K, b1=None, b2=0.0):
+    """Score, select on the (head-aggregated) score, gather (deep dive section 3.4)."""
     s, g = gate_score(h, W1, w2, instr_mask, b1, b2)
-    kept_idx, cu_kept = topk_select(s.astype(np.float32), instr_mask, cu_seqlens, K)
+    kept_idx, cu_kept = topk_select(aggregate_heads(s).astype(np.float32), instr_mask, cu_seqlens, K)
     h_k, p_k, g_k = gather_kept(h, pos, g, kept_idx, cu_seqlens)
     return {"s": s, "g": g, "kept_idx": kept_idx, "cu_kept": cu_kept,
             "h_kept": h_k, "pos_kept": p_k, "g_kept": g_k}
@@ -367,7 +409,7 @@ def gated_attention_bwd(Q, K, V, g, dO, cu_kept, tau, beta):
         for h in range(H_q):
             kv = h // group
             q, k, v, do = Q[a:e, h], K[a:e, kv], V[a:e, kv], dO[a:e, h]
-            bias = _log_bias(None if g is None else np.asarray(g)[a:e], float(beta[h]), n)
+            bias = _log_bias(_head_gate(g, h, H_q, a, e), float(beta[h]), n)
             x = np.where(causal, float(tau[h]) * c * (q @ k.T) + bias[None, :], -np.inf)
             mx = x.max(axis=1, keepdims=True)
             mx = np.where(np.isfinite(mx), mx, 0.0)
@@ -401,7 +443,7 @@ def gated_attention_lse(Q, K, g, cu_kept, tau, beta):
             continue
         causal = np.tril(np.ones((n, n), dtype=bool))
         for h in range(H_q):
-            bias = _log_bias(None if g is None else np.asarray(g)[a:e], float(beta[h]), n)
+            bias = _log_bias(_head_gate(g, h, H_q, a, e), float(beta[h]), n)
             x = np.where(causal, float(tau[h]) / math.sqrt(d_h) * (Q[a:e, h] @ K[a:e, h // group].T) + bias[None, :],
                          -np.inf)
             mx = x.max(axis=1)
@@ -413,8 +455,20 @@ def gated_attention_lse(Q, K, g, cu_kept, tau, beta):
 def gate_score_grad(dbias, beta, g_kept, kept_idx, T):
     """dL/ds for every input row: the kept row j carries dL/d(ln g_j) = sum_h beta_h dbias[j, h]
     and d ln g / ds = 1 - g for g = sigmoid(s); non-prunable rows have the constant g = 1 and
-    rows that were not kept get no gradient (the top-K choice itself has none)."""
-    dlng = np.asarray(dbias, dtype=np.float64) @ np.asarray(beta, dtype=np.float64)
-    ds = np.zeros(T)
-    ds[np.asarray(kept_idx, dtype=np.int64)] = dlng * (1.0 - np.asarray(g_kept, dtype=np.float64))
+    rows that were not kept get no gradient (the top-K choice itself has none).
+    Per-head gates g_kept [M, H_g]: gate head c collects the query heads that read it,
+    ds[:, c] = (1 - g[:, c]) sum_{h : gate_column(h) = c} beta_h dbias[:, h]; ds is [T, H_g]."""
+    dbias = np.asarray(dbias, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    g_kept = np.asarray(g_kept, dtype=np.float64)
+    kept_idx = np.asarray(kept_idx, dtype=np.int64)
+    if g_kept.ndim == 1:
+        ds = np.zeros(T)
+        ds[kept_idx] = (dbias @ beta) * (1.0 - g_kept)
+        return ds
+    H_q, H_g = dbias.shape[1], g_kept.shape[1]
+    ds = np.zeros((T, H_g))
+    for c in range(H_g):
+        heads = [h for h in range(H_q) if gate_column(h, H_q, H_g) == c]
+        ds[kept_idx, c] = (dbias[:, heads] @ beta[heads]) * (1.0 - g_kept[:, c])
     return ds

@@ -650,3 +650,171 @@ def test_planted_selection_mistake_fails_brute_force():
         kept_bad.extend(sorted(ranked + [j for j in rows if mask[j]]))
     ref, _ = _brute_force_keep(s, mask, cu, 5)
     assert kept_bad != ref.tolist()
+
+
+# ---------------------------------------------------------------------------
+# Per-head gate scores and uniform head aggregation (deep dive section 3.4)
+# ---------------------------------------------------------------------------
+
+def _heads_case(H_g, seed=61):
+    wl = I.WORKLOADS["tiny"]
+    gi = I.make_gate_inputs(wl)
+    rng = np.random.default_rng(seed)
+    h = I.bf16_bits_to_f64(gi["h"])
+    W1 = I.bf16_bits_to_f64(gi["W1"])
+    W2 = rng.standard_normal((H_g, wl.d_g)) * 0.05
+    b1 = rng.standard_normal(wl.d_g) * 0.1
+    b2 = rng.standard_normal(H_g) * 0.2
+    return wl, gi, h, W1, W2, b1, b2
+
+
+@pytest.mark.parametrize("H_g", [1, 2, 4])
+def test_gate_score_heads_match_torch_mlp(H_g):
+    wl, gi, h, W1, W2, b1, b2 = _heads_case(H_g)
+    s, g = O.gate_score(h, W1, W2, gi["instr_mask"], b1, b2)
+    assert s.shape == (wl.T_total, H_g) and g.shape == (wl.T_total, H_g)
+    hid = F.silu(F.linear(torch.from_numpy(h), torch.from_numpy(W1), torch.from_numpy(b1)))
+    ref_s = F.linear(hid, torch.from_numpy(W2), torch.from_numpy(b2))
+    ref_g = torch.sigmoid(ref_s)
+    ref_g[torch.from_numpy(gi["instr_mask"].astype(bool))] = 1.0
+    np.testing.assert_allclose(s, ref_s.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g, ref_g.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_uniform_aggregation_is_the_score_of_the_mean_head():
+    # the second layer is linear: the mean of H_g head scores is the single-head score of the
+    # mean row of W2 (and the mean b2); torch.mean gives the same row means
+    wl, gi, h, W1, W2, b1, b2 = _heads_case(4, seed=62)
+    s, _ = O.gate_score(h, W1, W2, gi["instr_mask"], b1, b2)
+    agg = O.aggregate_heads(s)
+    s1, _ = O.gate_score(h, W1, W2.mean(axis=0), gi["instr_mask"], b1, float(b2.mean()))
+    np.testing.assert_allclose(agg, s1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(agg, torch.from_numpy(s).mean(dim=1).numpy(), rtol=1e-14, atol=1e-14)
+    # one head: aggregation changes nothing
+    assert np.array_equal(O.aggregate_heads(s[:, 0]), s[:, 0])
+
+
+def test_per_head_normalisation_is_columnwise_unit_rms():
+    rng = np.random.default_rng(63)
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(30, 22), instr_lens=(4, 0), instr_where="scattered")
+    mask = I.make_instr_mask(wl)
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    s = rng.standard_normal((wl.T_total, 3)) * np.array([0.5, 3.0, 11.0])
+    b = O.normalize_scores(s, mask, cu, eps=0.0)
+    assert np.all(b[mask == 1] == 0.0)
+    for i in range(2):
+        doc = [j for j in range(cu[i], cu[i + 1]) if mask[j] == 0]
+        np.testing.assert_allclose(np.mean(b[doc] ** 2, axis=0), np.ones(3), rtol=1e-12)
+        # a per-head positive scale leaves the order within each head unchanged
+        for c in range(3):
+            assert np.array_equal(np.argsort(-s[doc, c], kind="stable"), np.argsort(-b[doc, c], kind="stable"))
+
+
+def _sdpa_reference_heads(Q, K, V, G, cu, tau, beta):
+    """torch CPU fp64 SDPA with a per-head additive mask; query head h adds beta_h ln of gate
+    column h * H_g // H_q."""
+    M, H_q, d_h = Q.shape
+    H_kv, H_g = K.shape[1], G.shape[1]
+    out = torch.zeros(M, H_q, d_h, dtype=torch.float64)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        if n == 0:
+            continue
+        causal = torch.full((n, n), float("-inf"), dtype=torch.float64).triu(1)
+        for h in range(H_q):
+            col = h * H_g // H_q
+            kv = h * H_kv // H_q
+            mask = causal + float(beta[h]) * torch.log(torch.from_numpy(G[a:e, col]))[None, :]
+            o = F.scaled_dot_product_attention(torch.from_numpy(Q[a:e, h])[None], torch.from_numpy(K[a:e, kv])[None],
+                                               torch.from_numpy(V[a:e, kv])[None], attn_mask=mask,
+                                               scale=float(tau[h]) / math.sqrt(d_h))
+            out[a:e, h] = o[0]
+    return out.numpy()
+
+
+@pytest.mark.parametrize("H_g", [2, 4])
+def test_attention_with_per_head_gates_matches_torch_sdpa(H_g):
+    Q, K, V, _, cu, tau, beta = _rand_attn(64, (9, 1, 15))
+    G = np.random.default_rng(65).uniform(0.02, 1.0, (Q.shape[0], H_g))
+    got = O.gated_attention(Q, K, V, G, cu, tau, beta)
+    np.testing.assert_allclose(got, _sdpa_reference_heads(Q, K, V, G, cu, tau, beta), rtol=1e-10, atol=1e-12)
+    # one gate column is the shared gate of the single-head form
+    np.testing.assert_allclose(O.gated_attention(Q, K, V, G[:, :1], cu, tau, beta),
+                               _sdpa_reference(Q, K, V, G[:, 0], cu, tau, beta), rtol=1e-10, atol=1e-12)
+
+
+def test_planted_gate_column_mistake_fails_the_sdpa_pin(monkeypatch):
+    # query heads spread over the gate heads modulo instead of in consecutive groups
+    Q, K, V, _, cu, tau, beta = _rand_attn(66, (13,))
+    G = np.random.default_rng(67).uniform(0.02, 1.0, (Q.shape[0], 2))
+    monkeypatch.setattr(O, "gate_column", lambda h, H_q, H_g: h % H_g)
+    got = O.gated_attention(Q, K, V, G, cu, tau, beta)
+    assert not np.allclose(got, _sdpa_reference_heads(Q, K, V, G, cu, tau, beta), rtol=1e-6, atol=1e-8)
+
+
+def test_eq8_attention_with_per_head_bias_matches_rowwise_sdpa():
+    Q, K, V, _, pos, cu, gain, temp = _eq8_case(68, (7, 12))
+    M, H_q, d_h = Q.shape
+    Bh = np.random.default_rng(69).standard_normal((M, 2))
+    got = O.gated_attention_eq8(Q, K, V, Bh, pos, cu, gain, temp)
+    # each query head is the single-bias form with its own column, which the row-wise torch pin checks
+    ref = np.zeros_like(got)
+    for h in range(H_q):
+        col = h * 2 // H_q
+        ref[:, h] = _sdpa_eq8_rows(Q, K, V, Bh[:, col], pos, cu, gain, temp)[:, h]
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def _torch_forward_heads(Q, K, V, G, cu, tau, beta):
+    """torch CPU fp64 forward with per-head gates, differentiable in Q, K, V and the bias."""
+    M, H_q, d_h = Q.shape
+    H_kv, H_g = K.shape[1], G.shape[1]
+    q, k, v = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (Q, K, V))
+    lng = torch.log(torch.tensor(G, dtype=torch.float64))
+    bias = torch.stack([float(beta[h]) * lng[:, h * H_g // H_q] for h in range(H_q)], dim=1)
+    bias = bias.detach().requires_grad_(True)
+    outs = []
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        mask = torch.full((n, n), float("-inf"), dtype=torch.float64).triu(1)
+        heads = []
+        for h in range(H_q):
+            kv = h * H_kv // H_q
+            z = (q[a:e, h] @ k[a:e, kv].T) * (float(tau[h]) / math.sqrt(d_h))
+            heads.append(torch.softmax(z + bias[a:e, h][None, :] + mask, dim=1) @ v[a:e, kv])
+        outs.append(torch.stack(heads, dim=1))
+    return torch.cat(outs, dim=0), (q, k, v, bias)
+
+
+def test_attention_bwd_with_per_head_gates_matches_torch_autograd():
+    Q, K, V, _, cu, tau, beta = _rand_attn(70, (8, 13))
+    G = np.random.default_rng(71).uniform(0.02, 1.0, (Q.shape[0], 4))
+    dO = np.random.default_rng(72).standard_normal(Q.shape)
+    dQ, dK, dV, dbias = O.gated_attention_bwd(Q, K, V, G, dO, cu, tau, beta)
+    out, (q, k, v, bias) = _torch_forward_heads(Q, K, V, G, cu, tau, beta)
+    (out * torch.from_numpy(dO)).sum().backward()
+    for got, ref in ((dQ, q.grad), (dK, k.grad), (dV, v.grad), (dbias, bias.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
+    lse = O.gated_attention_lse(Q, K, G, cu, tau, beta)
+    assert np.all(np.isfinite(lse))
+
+
+def test_gate_score_grad_per_head_by_finite_differences():
+    # ds[j, c] through g[:, c] = sigmoid(s[:, c]), for two gate heads shared by two query heads each
+    Q, K, V, _, cu, tau, beta = _rand_attn(73, (9,))
+    rng = np.random.default_rng(74)
+    S = rng.standard_normal((9, 2))
+    sig = lambda x: 1.0 / (1.0 + np.exp(-x))
+    dO = rng.standard_normal(Q.shape)
+    _, _, _, dbias = O.gated_attention_bwd(Q, K, V, sig(S), dO, cu, tau, beta)
+    kept = np.arange(9) * 3 + 1
+    ds = O.gate_score_grad(dbias, beta, sig(S), kept, 27)
+    assert ds.shape == (27, 2) and np.all(np.delete(ds, kept, axis=0) == 0.0)
+    loss = lambda SS: float(np.sum(dO * O.gated_attention(Q, K, V, sig(SS), cu, tau, beta)))
+    for j, c in ((0, 0), (4, 1), (8, 1), (3, 0)):
+        up, dn = S.copy(), S.copy()
+        up[j, c] += 1e-6
+        dn[j, c] -= 1e-6
+        assert abs((loss(up) - loss(dn)) / 2e-6 - ds[kept[j], c]) < 1e-6
