@@ -587,6 +587,109 @@ def two_budget(path, torch, flush, steps):
                     "a separate full-budget attention call; host launches inside the events"}
 
 
+def backward(path, torch, flush, steps):
+    """Next-row backward on the bench batch's kept rows: the forward with its log-sum-exp,
+    the attention backward (dQ, dK, dV and the bias gradient, fp32 CUDA-core kernels) and
+    the chain to the gate scores. Algorithmic FLOPs of the backward: 10 d_h per visible
+    (query, key) pair per query head (S = QK^T recomputed once, dV, dP, dQ, dK)."""
+    from learned_token_pruning_07_b300 import binding as tg
+    wl, d, M = path.wl, path.d, path.M
+    path.step()  # fills cu_kept, kept, g_kept for this batch
+    e = lambda *shape, dt=torch.float32: torch.empty(*shape, dtype=dt, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(wl.seed + 11)
+    dO = torch.randn((M, wl.H_q, wl.d_h), generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16)
+    lse = e(M, wl.H_q)
+    dQ, dK, dV = e(M, wl.H_q, wl.d_h), e(M, wl.H_kv, wl.d_h), e(M, wl.H_kv, wl.d_h)
+    dbias, ds = e(M, wl.H_q), e(wl.T_total)
+    g_kept = path.g_kept[:M]
+
+    def fwd():
+        tg.gated_attention_lse(d["Q"], d["K"], d["V"], path.cu_kept, path.tau, path.beta, path.O, lse,
+                               max_seqlen=path.max_seqlen, g=g_kept, status=path.status)
+
+    def bwd():
+        tg.gated_attention_bwd(d["Q"], d["K"], d["V"], path.O, dO, lse, path.cu_kept, path.tau, path.beta,
+                               dQ, dK, dV, dbias, max_seqlen=path.max_seqlen, g=g_kept, status=path.status)
+
+    def chain():
+        tg.gate_score_grad(dbias, path.beta, g_kept, path.kept[:M], path.cu_kept, ds)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, min(steps, 10))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1000.0)
+        return float(np.median(ts))
+
+    f_us, b_us, c_us = timed(fwd), timed(bwd), timed(chain)
+    assert tg.read_device_status(path.status) == 0, "device reported an error"
+    pairs = sum(n * (n + 1) // 2 for n in path.kept_lens)
+    bwd_flops = 10.0 * wl.d_h * wl.H_q * pairs
+    del dO, lse, dQ, dK, dV, dbias, ds
+    torch.cuda.empty_cache()
+    return {"forward_lse_us": f_us, "attention_bwd_us": b_us, "gate_score_grad_us": c_us,
+            "attention_bwd_tflops": bwd_flops / (b_us * 1e-6) / 1e12,
+            "note": "fp32 CUDA-core backward (no tensor cores); single launches with events around each, "
+                    "L2 flushed before each"}
+
+
+def heads(path, torch, flush, steps):
+    """Per-head gates on the bench batch: scoring with H_g = 16 gate heads (per-head scores and
+    gates plus the head mean that selection ranks) against the single-gate score, and the
+    attention with one gate column per query head against the shared gate."""
+    from learned_token_pruning_07_b300 import binding as tg
+    from learned_token_pruning_07_b300 import inputs as I
+    wl, d, T, H_g = path.wl, path.d, path.wl.T_total, path.wl.H_q
+    hw = I.make_gate_head_weights(wl, H_g)
+    W2 = torch.from_numpy(hw["W2"].view(np.int16)).cuda()
+    e = lambda *shape: torch.empty(*shape, dtype=torch.float32, device="cuda")
+    s_h, g_h, sel = e(T, H_g), e(T, H_g), e(T)
+    G = torch.from_numpy(I.make_head_gates(wl, path.M, H_g)).cuda()
+
+    def score_heads():
+        tg.gate_score_heads(d["h"], path.W1, W2, s_h, sel, g_heads=g_h, instr_mask=d["mask"], b2=hw["b2"],
+                            status=path.status)
+
+    def score_one():
+        tg.gate_score(d["h"], path.W1, path.w2, path.s, path.g, instr_mask=d["mask"], status=path.status)
+
+    def attn_heads():
+        tg.gated_attention(d["Q"], d["K"], d["V"], path.cu_kept, path.tau, path.beta, path.O,
+                           max_seqlen=path.max_seqlen, g=G, status=path.status)
+
+    def attn_one():
+        tg.gated_attention(d["Q"], d["K"], d["V"], path.cu_kept, path.tau, path.beta, path.O,
+                           max_seqlen=path.max_seqlen, g=path.g_kept, status=path.status)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, min(steps, 20))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1000.0)
+        return float(np.median(ts))
+
+    path.step()  # cu_kept and g_kept for the kept rows
+    out = {"H_g": H_g, "gate_score_heads_us": timed(score_heads), "gate_score_us": timed(score_one),
+           "attention_per_head_gates_us": timed(attn_heads), "attention_shared_gate_us": timed(attn_one),
+           "note": "single launches with events around each (launch gap included), L2 flushed before each"}
+    assert tg.read_device_status(path.status) == 0, "device reported an error"
+    return out
+
+
 def workload_label(wl, K):
     docs = wl.doc_lens if wl.B > 1 else wl.doc_lens[0]
     ins = wl.instr_lens if wl.B > 1 else wl.instr_lens[0]
@@ -724,6 +827,8 @@ def run_gpu(args, rank, world, local):
 
     paper = paper_form(path, torch, flush, args.steps) if rank == 0 else None
     twob = two_budget(path, torch, flush, args.steps) if rank == 0 else None
+    bwd = backward(path, torch, flush, args.steps) if rank == 0 else None
+    hds = heads(path, torch, flush, args.steps) if rank == 0 else None
     longctx = long_context(torch, flush, args.steps) if (args.long_context and rank == 0) else None
 
     cpu = None
@@ -759,6 +864,10 @@ def run_gpu(args, rank, world, local):
             line["paper_form"] = paper
         if twob:
             line["two_budget"] = twob
+        if bwd:
+            line["backward"] = bwd
+        if hds:
+            line["heads"] = hds
         if longctx:
             line["long_context"] = longctx
         print(json.dumps(line), flush=True)

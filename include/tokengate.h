@@ -108,6 +108,24 @@ TG_API tg_status tg_gate_score_rmsnorm(const uint16_t *h, int32_t T_total, int32
                                 float *g_out, int32_t *status, tg_stream_t stream);
 
 /*
+ * tg_gate_score_heads — per-head gate scores (deep dive section 3.4: the gate carries a
+ *   per-head bias, and selection aggregates the heads uniformly):
+ *     u = W1 a_j (+ b1), s_jc = W2[c] . SiLU(u) (+ b2[c]), g_jc = sigmoid(s_jc) (1 on
+ *     non-prunable rows), s_sel_j = (1/H_g) sum_c s_jc (summed in head order in fp32).
+ *   W2 [device] bf16 [H_g, d_g], row c the second layer of gate head c; b2 [host] fp32 [H_g]
+ *   or NULL. 1 <= H_g <= 16 (else TG_ERR_UNSUPPORTED).
+ *   rmsnorm: 0, or 1 for LN_2 fused in front (then W1 is the folded weight and h the raw
+ *   residual, as tg_gate_score_rmsnorm; ln_eps finite, >= 0).
+ *   s_heads [device] fp32 [T_total, H_g]; g_heads [device] fp32 [T_total, H_g] or NULL;
+ *   s_sel [device] fp32 [T_total] (required): the row mean that tg_topk_select ranks.
+ *   Other arguments, shapes and errors as tg_gate_score.
+ */
+TG_API tg_status tg_gate_score_heads(const uint16_t *h, int32_t T_total, int32_t d, const uint8_t *instr_mask,
+                              const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
+                              int32_t d_g, int32_t H_g, int32_t rmsnorm, float ln_eps, float *s_heads,
+                              float *g_heads, float *s_sel, int32_t *status, tg_stream_t stream);
+
+/*
  * tg_fold_rmsnorm_weight — W1_out[k, c] = bf16(W1[k, c] * ln_weight[c]) (round to nearest
  *   even), the weight tg_gate_score_rmsnorm takes. W1 [device] bf16 [d_g, d]; ln_weight
  *   [device] bf16 [d]; W1_out [device] bf16 [d_g, d] (may not alias W1). Run once per weight.
@@ -140,13 +158,14 @@ TG_API tg_status tg_topk_select(const float *s, const uint8_t *instr_mask, const
  *   position_ids[:, keep]; paper page Figure 1 (b): kept states travel with their scores).
  *   h        [device] bf16 [T_total, d], 16-byte aligned rows (d % 8 == 0).
  *   pos      [device] int32 [T_total] or NULL (then pos = row - cu_seqlens[b]).
- *   g        [device] fp32 [T_total] or NULL (then g_kept is not written).
+ *   g        [device] fp32 [T_total, H_g] or NULL (then g_kept is not written); H_g gate
+ *            values per row (1 <= H_g <= 16; 1 for the single gate).
  *   kept_idx, cu_kept as written by tg_topk_select; rows m < min(cu_kept[B], capacity).
  *   h_kept   [device] bf16 [capacity, d].  pos_kept [device] int32 [capacity] or NULL.
- *   g_kept   [device] fp32 [capacity] or NULL.
+ *   g_kept   [device] fp32 [capacity, H_g] or NULL.
  *   status   [device] int32 word (TG_DEV_BAD_INDEX) or NULL.
  */
-TG_API tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g,
+TG_API tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g, int32_t H_g,
                          const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
                          const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                          uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
@@ -161,7 +180,9 @@ TG_API tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const flo
  *   Query head h reads kv head h / (H_q / H_kv). A query whose every key has zero weight
  *   outputs zeros.
  *   Q [device] bf16 [M, H_q, d_h];  K, V [device] bf16 [M, H_kv, d_h]; token-major, dense.
- *   g [device] fp32 [M] or NULL (no bias).
+ *   g [device] fp32 [M, H_g] or NULL (no bias). Per-head gates (deep dive section 3.4: a
+ *     per-head bias): query head h reads g[j, h / (H_q / H_g)]; H_g = 1 is the shared gate.
+ *     1 <= H_g <= 16 and H_q % H_g == 0 (else TG_ERR_UNSUPPORTED); pass 1 when g is NULL.
  *   cu_kept [device] int32 [B+1]: sequence boundaries in the kept rows; rows are clamped
  *     to M_capacity.
  *   max_seqlen: host upper bound on any cu_kept[b+1] - cu_kept[b] (sizes the grid;
@@ -172,7 +193,7 @@ TG_API tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const flo
  *   Compute: bf16 tcgen05 MMA, fp32 softmax and accumulation.
  */
 TG_API tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                             const float *g, const int32_t *cu_kept, int32_t B,
+                             const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                              int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                              int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                              int32_t *status, tg_stream_t stream);
@@ -184,7 +205,7 @@ TG_API tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const 
  *   lse [device] fp32 [M_capacity, H_q]. Other arguments as tg_gated_attention.
  */
 TG_API tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                                  float *lse, int32_t *status, tg_stream_t stream);
@@ -203,7 +224,7 @@ TG_API tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, co
  *   fp32 (64x64 tiles recomputed in shared memory). Other arguments as tg_gated_attention.
  */
 TG_API tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const uint16_t *O, const uint16_t *dO,
+                                 const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,
                                  const float *lse, const int32_t *cu_kept, int32_t B,
                                  int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, float *dQ,
@@ -212,12 +233,15 @@ TG_API tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, co
 
 /*
  * tg_gate_score_grad — carry the attention bias gradient back to the gate scores:
- *   ds[kept_idx[m]] = (1 - g_kept[m]) * sum_h beta_h dbias[m, h] for m < min(cu_kept[B], capacity)
- *   (d ln g / ds = 1 - g for g = sigmoid(s); non-prunable rows have g = 1, so they get 0).
- *   Rows that were not kept are not written: the caller zeroes ds [device] fp32 [T_total].
- *   dbias [device] fp32 [capacity, H_q]; beta [host] fp32 [H_q]; g_kept [device] fp32 [capacity].
+ *   ds[kept_idx[m], c] = (1 - g_kept[m, c]) * sum over the query heads h that read gate head c
+ *   of beta_h dbias[m, h], for m < min(cu_kept[B], capacity) (d ln g / ds = 1 - g for
+ *   g = sigmoid(s); non-prunable rows have g = 1, so they get 0). With H_g = 1 every head
+ *   reads the one gate. Rows that were not kept are not written: the caller zeroes
+ *   ds [device] fp32 [T_total, H_g].
+ *   dbias [device] fp32 [capacity, H_q]; beta [host] fp32 [H_q];
+ *   g_kept [device] fp32 [capacity, H_g]; 1 <= H_g <= 16, H_q % H_g == 0.
  */
-TG_API tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+TG_API tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept, int32_t H_g,
                              const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
                              int32_t capacity, int32_t H_q, int32_t T_total, float *ds,
                              tg_stream_t stream);
@@ -235,6 +259,20 @@ TG_API tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, cons
                               int32_t *kept_idx, int32_t capacity, int32_t *cu_kept,
                               uint16_t *h_kept, int32_t *pos_kept, float *g_kept,
                               int32_t *status, tg_stream_t stream);
+
+/*
+ * tg_gate_prune_layer_heads — the prune path with per-head gates: tg_gate_score_heads, then
+ *   tg_topk_select on the head mean s_sel, then tg_gather_kept of the H_g gate values per
+ *   kept row (g_kept [device] fp32 [capacity, H_g]). Arguments as in those calls; s_heads,
+ *   g_heads and s_sel are required here.
+ */
+TG_API tg_status tg_gate_prune_layer_heads(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                                    const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                                    const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
+                                    int32_t d_g, int32_t H_g, int32_t K, float *s_heads, float *g_heads,
+                                    float *s_sel, int32_t *kept_idx, int32_t capacity, int32_t *cu_kept,
+                                    uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
+                                    tg_stream_t stream);
 
 /*
  * tg_two_budget_prune_layer — the packed two-budget forward of training (deep dive section 3.3,
@@ -274,14 +312,20 @@ TG_API tg_status tg_apply_rope(uint16_t *X, const int32_t *pos, const int32_t *c
  *   3.1, Eq. (3)): b_j = s_j / sqrt(mean over the sequence's prunable rows of s^2 + eps), and
  *   b_j = 0 on non-prunable rows. A sequence without prunable rows gets b = 0. The order of
  *   the prunable scores is unchanged, so top-K may select from s or from b alike.
- *   s [device] fp32 [T_total] (as written by tg_gate_score); instr_mask [device] uint8 or NULL;
+ *   s [device] fp32 [T_total, H_g] (as written by tg_gate_score / tg_gate_score_heads); each
+ *   gate head is normalised on its own. instr_mask [device] uint8 or NULL;
  *   cu_seqlens [device] int32 [B+1]; eps: host, finite, >= 0 (the pages give none; 1e-6 is the
- *   usual choice). b_out [device] fp32 [T_total]. status [device] int32 word (TG_DEV_BAD_SEQLENS).
- *   Limits: 1 <= B <= 1024. The per-sequence sum runs in a fixed order (deterministic).
+ *   usual choice). b_out [device] fp32 [T_total, H_g].
+ *   b_sel [device] fp32 [T_total] or NULL: with H_g > 1, the row mean of the normalised heads
+ *   (the uniform head aggregation that top-K ranks; 0 on non-prunable rows). Not written when
+ *   H_g = 1 (b_out itself is then the ranking).
+ *   status [device] int32 word (TG_DEV_BAD_SEQLENS).
+ *   Limits: 1 <= B <= 1024, 1 <= H_g <= 16. The per-sequence sums run in a fixed order
+ *   (deterministic).
  */
-TG_API tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
-                              int32_t B, int32_t T_total, float eps, float *b_out, int32_t *status,
-                              tg_stream_t stream);
+TG_API tg_status tg_normalize_scores(const float *s, int32_t H_g, const uint8_t *instr_mask,
+                              const int32_t *cu_seqlens, int32_t B, int32_t T_total, float eps,
+                              float *b_out, float *b_sel, int32_t *status, tg_stream_t stream);
 
 /*
  * tg_gated_attention_eq8 — the operative token-gated attention of the deep dive, section 3.2,
@@ -291,14 +335,15 @@ TG_API tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, 
  *   m_i = number of retained keys query i sees (its index in the kept sequence + 1),
  *   p_i = number of positions it originally saw (its original position id + 1).
  *   gain_h = softplus(gamma_h) and temp_h = softplus(sigma_h) are passed already transformed.
- *   b   [device] fp32 [M]: normalised scores of the kept rows (tg_normalize_scores, gathered by
- *       tg_gather_kept), or NULL for no score bias.
+ *   b   [device] fp32 [M, H_g]: normalised scores of the kept rows (tg_normalize_scores,
+ *       gathered by tg_gather_kept), or NULL for no score bias; query head h reads gate head
+ *       h / (H_q / H_g) (1 <= H_g <= 16, H_q % H_g == 0; pass 1 when b is NULL).
  *   pos [device] int32 [M]: original position ids of the kept rows (tg_gather_kept's pos_kept).
  *   gain, temp [host] fp32 [H_q], finite and >= 0.
  *   Other arguments, layouts, shapes and errors as tg_gated_attention.
  */
 TG_API tg_status tg_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                 const float *b, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
                                  int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q,
                                  int32_t H_kv, int32_t d_h, const float *gain, const float *temp,
                                  uint16_t *O, int32_t *status, tg_stream_t stream);

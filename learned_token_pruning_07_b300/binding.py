@@ -31,19 +31,22 @@ SIGNATURES = {
     "tg_gate_score_rmsnorm": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _I, _F, _P, _P, _P, _P]),
     "tg_fold_rmsnorm_weight": (_I, [_P, _P, _I, _I, _P, _P]),
     "tg_topk_select": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
-    "tg_gather_kept": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
-    "tg_gated_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
-    "tg_gated_attention_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-    "tg_gated_attention_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
-                                    _P, _P, _P]),
-    "tg_gate_score_grad": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "tg_gate_score_heads": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "tg_gather_kept": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "tg_gated_attention": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_gated_attention_lse": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "tg_gated_attention_bwd": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                    _P, _P, _P, _P]),
+    "tg_gate_score_grad": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "tg_gate_prune_layer_heads": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P,
+                                       _I, _P, _P, _P, _P, _P, _P]),
     "tg_gate_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
                                  _P, _P, _P, _P, _P, _P]),
     "tg_two_budget_prune_layer": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _I,
                                        _P, _P, _P, _P, _P, _P]),
     "tg_apply_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P]),
-    "tg_normalize_scores": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P]),
-    "tg_gated_attention_eq8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_normalize_scores": (_I, [_P, _I, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
+    "tg_gated_attention_eq8": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tg_read_device_status": (_I, [_P, _P, _P]),
     "tg_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "tg_set_test_withhold": (_I, [_I]),
@@ -97,6 +100,11 @@ def _check(name: str, status: int):
         raise TGError(name, status, msg)
 
 
+def _heads(g) -> int:
+    """Gate heads of a gate tensor: [rows] is one head, [rows, H_g] is H_g."""
+    return 1 if g is None or g.dim() == 1 else int(g.shape[1])
+
+
 def _host_f32(x):
     import numpy as np
     a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
@@ -114,6 +122,19 @@ def gate_score(h, W1, w2, s_out, g_out=None, instr_mask=None, b1=None, b2: float
     st = load().tg_gate_score(_ptr(h), T, d, _ptr(instr_mask), _ptr(W1), _ptr(b1), _ptr(w2), float(b2),
                               d_g, _ptr(s_out), _ptr(g_out), _ptr(status), _stream(stream))
     _check("tg_gate_score", st)
+
+
+def gate_score_heads(h, W1, W2, s_heads, s_sel, g_heads=None, instr_mask=None, b1=None, b2=None,
+                     rmsnorm: bool = False, ln_eps: float = 1e-6, status=None, stream=None):
+    """Per-head scores s_heads [T, H_g], gates g_heads and their head mean s_sel [T]."""
+    T, d = h.shape
+    H_g, d_g = W2.shape
+    b2_a, b2_p = _host_f32(b2) if b2 is not None else (None, None)
+    st = load().tg_gate_score_heads(_ptr(h), T, d, _ptr(instr_mask), _ptr(W1), _ptr(b1), _ptr(W2), b2_p, d_g,
+                                    H_g, int(bool(rmsnorm)), float(ln_eps), _ptr(s_heads), _ptr(g_heads),
+                                    _ptr(s_sel), _ptr(status), _stream(stream))
+    del b2_a
+    _check("tg_gate_score_heads", st)
 
 
 def gate_score_rmsnorm(h, W1_folded, w2, s_out, g_out=None, instr_mask=None, b1=None, b2: float = 0.0,
@@ -144,7 +165,7 @@ def gather_kept(h, cu_seqlens, kept_idx, cu_kept, h_kept, pos=None, g=None, pos_
                 g_kept=None, status=None, stream=None):
     T, d = h.shape
     B = cu_seqlens.numel() - 1
-    st = load().tg_gather_kept(_ptr(h), _ptr(pos), _ptr(g), _ptr(cu_seqlens), B, T, d, _ptr(kept_idx),
+    st = load().tg_gather_kept(_ptr(h), _ptr(pos), _ptr(g), _heads(g), _ptr(cu_seqlens), B, T, d, _ptr(kept_idx),
                                _ptr(cu_kept), h_kept.shape[0], _ptr(h_kept), _ptr(pos_kept),
                                _ptr(g_kept), _ptr(status), _stream(stream))
     _check("tg_gather_kept", st)
@@ -157,17 +178,18 @@ def gated_attention(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, sta
     B = cu_kept.numel() - 1
     tau_a, tau_p = _host_f32(tau)
     beta_a, beta_p = _host_f32(beta)
-    st = load().tg_gated_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(cu_kept), B, M,
+    st = load().tg_gated_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept), B, M,
                                    int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O),
                                    _ptr(status), _stream(stream))
     del tau_a, beta_a
     _check("tg_gated_attention", st)
 
 
-def normalize_scores(s, cu_seqlens, b_out, instr_mask=None, eps: float = 1e-6, status=None, stream=None):
+def normalize_scores(s, cu_seqlens, b_out, instr_mask=None, eps: float = 1e-6, b_sel=None, status=None,
+                     stream=None):
     B = cu_seqlens.numel() - 1
-    st = load().tg_normalize_scores(_ptr(s), _ptr(instr_mask), _ptr(cu_seqlens), B, s.numel(), float(eps),
-                                    _ptr(b_out), _ptr(status), _stream(stream))
+    st = load().tg_normalize_scores(_ptr(s), _heads(s), _ptr(instr_mask), _ptr(cu_seqlens), B, s.shape[0],
+                                    float(eps), _ptr(b_out), _ptr(b_sel), _ptr(status), _stream(stream))
     _check("tg_normalize_scores", st)
 
 
@@ -178,7 +200,7 @@ def gated_attention_eq8(Q, K, V, cu_kept, pos, gain, temp, O, max_seqlen: int, b
     B = cu_kept.numel() - 1
     gain_a, gain_p = _host_f32(gain)
     temp_a, temp_p = _host_f32(temp)
-    st = load().tg_gated_attention_eq8(_ptr(Q), _ptr(K), _ptr(V), _ptr(b), _ptr(pos), _ptr(cu_kept), B, M,
+    st = load().tg_gated_attention_eq8(_ptr(Q), _ptr(K), _ptr(V), _ptr(b), _heads(b), _ptr(pos), _ptr(cu_kept), B, M,
                                        int(max_seqlen), H_q, H_kv, d_h, gain_p, temp_p, _ptr(O), _ptr(status),
                                        _stream(stream))
     del gain_a, temp_a
@@ -189,7 +211,8 @@ def gated_attention_lse(Q, K, V, cu_kept, tau, beta, O, lse, max_seqlen: int, g=
     M, H_q, d_h = Q.shape
     tau_a, tau_p = _host_f32(tau)
     beta_a, beta_p = _host_f32(beta)
-    st = load().tg_gated_attention_lse(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(cu_kept), cu_kept.numel() - 1, M,
+    st = load().tg_gated_attention_lse(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept),
+                                       cu_kept.numel() - 1, M,
                                        int(max_seqlen), H_q, K.shape[1], d_h, tau_p, beta_p, _ptr(O), _ptr(lse),
                                        _ptr(status), _stream(stream))
     del tau_a, beta_a
@@ -201,7 +224,7 @@ def gated_attention_bwd(Q, K, V, O, dO, lse, cu_kept, tau, beta, dQ, dK, dV, dbi
     M, H_q, d_h = Q.shape
     tau_a, tau_p = _host_f32(tau)
     beta_a, beta_p = _host_f32(beta)
-    st = load().tg_gated_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _ptr(O), _ptr(dO), _ptr(lse),
+    st = load().tg_gated_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(O), _ptr(dO), _ptr(lse),
                                        _ptr(cu_kept), cu_kept.numel() - 1, M, int(max_seqlen), H_q, K.shape[1],
                                        d_h, tau_p, beta_p, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbias),
                                        _ptr(status), _stream(stream))
@@ -212,8 +235,8 @@ def gated_attention_bwd(Q, K, V, O, dO, lse, cu_kept, tau, beta, dQ, dK, dV, dbi
 def gate_score_grad(dbias, beta, g_kept, kept_idx, cu_kept, ds, stream=None):
     H_q = dbias.shape[1]
     beta_a, beta_p = _host_f32(beta)
-    st = load().tg_gate_score_grad(_ptr(dbias), beta_p, _ptr(g_kept), _ptr(kept_idx), _ptr(cu_kept),
-                                   cu_kept.numel() - 1, kept_idx.numel(), H_q, ds.numel(), _ptr(ds),
+    st = load().tg_gate_score_grad(_ptr(dbias), beta_p, _ptr(g_kept), _heads(g_kept), _ptr(kept_idx),
+                                   _ptr(cu_kept), cu_kept.numel() - 1, kept_idx.numel(), H_q, ds.shape[0], _ptr(ds),
                                    _stream(stream))
     del beta_a
     _check("tg_gate_score_grad", st)
@@ -230,6 +253,22 @@ def gate_prune_layer(h, cu_seqlens, W1, w2, K: int, s_out, g_out, kept_idx, cu_k
                                     _ptr(cu_kept), _ptr(h_kept), _ptr(pos_kept), _ptr(g_kept),
                                     _ptr(status), _stream(stream))
     _check("tg_gate_prune_layer", st)
+
+
+def gate_prune_layer_heads(h, cu_seqlens, W1, W2, K: int, s_heads, g_heads, s_sel, kept_idx, cu_kept, h_kept,
+                           pos_kept=None, g_kept=None, pos=None, instr_mask=None, b1=None, b2=None,
+                           status=None, stream=None):
+    T, d = h.shape
+    B = cu_seqlens.numel() - 1
+    H_g, d_g = W2.shape
+    b2_a, b2_p = _host_f32(b2) if b2 is not None else (None, None)
+    st = load().tg_gate_prune_layer_heads(_ptr(h), _ptr(pos), _ptr(instr_mask), _ptr(cu_seqlens), B, T, d,
+                                          _ptr(W1), _ptr(b1), _ptr(W2), b2_p, d_g, H_g, int(K), _ptr(s_heads),
+                                          _ptr(g_heads), _ptr(s_sel), _ptr(kept_idx), kept_idx.numel(),
+                                          _ptr(cu_kept), _ptr(h_kept), _ptr(pos_kept), _ptr(g_kept),
+                                          _ptr(status), _stream(stream))
+    del b2_a
+    _check("tg_gate_prune_layer_heads", st)
 
 
 def two_budget_prune_layer(h, cu_seqlens, W1, w2, K_prune: int, s_out, g_out, kept_idx, cu_packed, h_kept,

@@ -8,13 +8,14 @@ namespace tg_host {
 tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8_t *mask,
                             const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
                             int32_t d_g, float *s_out, float *g_out, int32_t *status,
-                            cudaStream_t stream, bool rmsnorm, float ln_eps);
+                            cudaStream_t stream, bool rmsnorm, float ln_eps, int32_t H_g = 1,
+                            const float *b2h = nullptr, float *s_sel = nullptr);
 tg_status launch_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_w, int32_t d_g, int32_t d,
                                      uint16_t *W1_out, cudaStream_t stream);
 tg_status launch_topk_select(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
                              int32_t B, int32_t T, int32_t K, int32_t *kept_idx, int32_t capacity,
                              int32_t *cu_kept, int32_t *status, cudaStream_t stream, int32_t cu_base = 0);
-tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
+tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g, int32_t H_g,
                         const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t d,
                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
@@ -24,27 +25,27 @@ tg_status launch_two_budget_prologue(const int32_t *cu_seqlens, int32_t B, int32
 tg_status launch_rope(uint16_t *X, const int32_t *pos, const int32_t *cu_kept, int32_t B,
                       int32_t capacity, int32_t H, int32_t d_h, float theta, cudaStream_t stream);
 tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                                  int32_t *status, cudaStream_t stream, float *lse = nullptr);
 tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                     const float *g, const uint16_t *O, const uint16_t *dO,
+                                     const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,
                                      const float *lse, const int32_t *cu_kept, int32_t B, int32_t M_cap,
                                      int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h,
                                      const float *tau, const float *beta, float *dQ, float *dK, float *dV,
                                      float *dbias, int32_t *status, cudaStream_t stream);
-tg_status launch_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+tg_status launch_gate_score_grad(const float *dbias, const float *beta, const float *g_kept, int32_t H_g,
                                  const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
                                  int32_t capacity, int32_t H_q, int32_t T, float *ds, cudaStream_t stream);
 tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                     const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                     const float *b, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
                                      int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q,
                                      int32_t H_kv, int32_t d_h, const float *gain,
                                      const float *temp, uint16_t *O, int32_t *status,
                                      cudaStream_t stream);
-tg_status launch_normalize_scores(const float *s, const uint8_t *mask, const int32_t *cu_seqlens,
-                                  int32_t B, int32_t T, float eps, float *b_out, int32_t *status,
+tg_status launch_normalize_scores(const float *s, int32_t H_g, const uint8_t *mask, const int32_t *cu_seqlens,
+                                  int32_t B, int32_t T, float eps, float *b_out, float *b_sel, int32_t *status,
                                   cudaStream_t stream);
 }  // namespace tg_host
 
@@ -54,6 +55,14 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline cudaStream_t S(tg_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 constexpr int32_t kMaxSelectB = 1024;
+constexpr int32_t kMaxGateHeads = 16;
+
+// H_g gate heads: 1 <= H_g <= 16, and the query heads split evenly over them
+tg_status check_gate_heads(int32_t H_g, int32_t H_q) {
+  if (H_g < 1) return TG_ERR_INVALID_ARG;
+  if (H_g > kMaxGateHeads || (H_q > 0 && H_q % H_g != 0)) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
 
 tg_status check_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint16_t *W1,
                            const uint16_t *w2, int32_t d_g, const float *s_out, float b2) {
@@ -107,6 +116,21 @@ tg_status tg_gate_score_rmsnorm(const uint16_t *h, int32_t T_total, int32_t d,
                                     status, S(stream), true, ln_eps);
 }
 
+tg_status tg_gate_score_heads(const uint16_t *h, int32_t T_total, int32_t d, const uint8_t *instr_mask,
+                              const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
+                              int32_t d_g, int32_t H_g, int32_t rmsnorm, float ln_eps, float *s_heads,
+                              float *g_heads, float *s_sel, int32_t *status, tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1, W2, d_g, s_heads, 0.0f);
+  if (st == TG_OK) st = check_gate_heads(H_g, 0);
+  if (st != TG_OK) return st;
+  if (!s_sel || (rmsnorm != 0 && rmsnorm != 1)) return TG_ERR_INVALID_ARG;
+  if (rmsnorm && (!std::isfinite(ln_eps) || ln_eps < 0.0f)) return TG_ERR_INVALID_ARG;
+  for (int c = 0; b2 && c < H_g; ++c)
+    if (!std::isfinite(b2[c])) return TG_ERR_INVALID_ARG;
+  return tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, W2, b2 ? b2[0] : 0.0f, d_g, s_heads,
+                                    g_heads, status, S(stream), rmsnorm != 0, ln_eps, H_g, b2, s_sel);
+}
+
 tg_status tg_fold_rmsnorm_weight(const uint16_t *W1, const uint16_t *ln_weight, int32_t d_g, int32_t d,
                                  uint16_t *W1_out, tg_stream_t stream) {
   if (!W1 || !ln_weight || !W1_out || d_g <= 0 || d <= 0) return TG_ERR_INVALID_ARG;
@@ -122,22 +146,24 @@ tg_status tg_topk_select(const float *s, const uint8_t *instr_mask, const int32_
                                      cu_kept, status, S(stream));
 }
 
-tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g,
+tg_status tg_gather_kept(const uint16_t *h, const int32_t *pos, const float *g, int32_t H_g,
                          const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
                          const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                          uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
                          tg_stream_t stream) {
   tg_status st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity, h_kept);
+  if (st == TG_OK) st = check_gate_heads(H_g, 0);
   if (st != TG_OK) return st;
-  return tg_host::launch_gather(h, pos, g, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity,
+  return tg_host::launch_gather(h, pos, g, H_g, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity,
                                 h_kept, pos_kept, g_kept, status, S(stream));
 }
 
 namespace {
-tg_status check_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *cu_kept,
-                          int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
-                          int32_t d_h, const float *tau, const float *beta, const void *O) {
-  if (!Q || !K || !V || !cu_kept || !tau || !beta || !O) return TG_ERR_INVALID_ARG;
+tg_status check_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int32_t H_g,
+                          const int32_t *cu_kept, int32_t B, int32_t M_capacity, int32_t max_seqlen,
+                          int32_t H_q, int32_t H_kv, int32_t d_h, const float *tau, const float *beta,
+                          const void *O) {
+  if (!Q || !K || !V || !cu_kept || !tau || !beta || !O || H_g < 1) return TG_ERR_INVALID_ARG;
   if (B < 1 || M_capacity < 0 || max_seqlen < 0 || H_q < 1 || H_kv < 1 || d_h < 1)
     return TG_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TG_ERR_INVALID_ARG;
@@ -146,49 +172,49 @@ tg_status check_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *
     if (!std::isfinite(beta[h]) || beta[h] < 0.0f) return TG_ERR_INVALID_ARG;
   }
   if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
-  return TG_OK;
+  return check_gate_heads(H_g, H_q);
 }
 }  // namespace
 
 tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                             const float *g, const int32_t *cu_kept, int32_t B,
+                             const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                              int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                              int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                              int32_t *status, tg_stream_t stream) {
-  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  tg_status st = check_attention(Q, K, V, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
   if (st != TG_OK) return st;
-  return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
+  return tg_host::launch_gated_attention(Q, K, V, g, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
                                          d_h, tau, beta, O, status, S(stream));
 }
 
 tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                                  float *lse, int32_t *status, tg_stream_t stream) {
-  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  tg_status st = check_attention(Q, K, V, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
   if (st == TG_OK && !lse) st = TG_ERR_INVALID_ARG;
   if (st != TG_OK) return st;
-  return tg_host::launch_gated_attention(Q, K, V, g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
+  return tg_host::launch_gated_attention(Q, K, V, g, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
                                          d_h, tau, beta, O, status, S(stream), lse);
 }
 
 tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const uint16_t *O, const uint16_t *dO,
+                                 const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,
                                  const float *lse, const int32_t *cu_kept, int32_t B,
                                  int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, float *dQ,
                                  float *dK, float *dV, float *dbias, int32_t *status,
                                  tg_stream_t stream) {
-  tg_status st = check_attention(Q, K, V, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  tg_status st = check_attention(Q, K, V, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
   if (st == TG_OK && (!dO || !lse || !dQ || !dK || !dV || !dbias)) st = TG_ERR_INVALID_ARG;
   if (st != TG_OK) return st;
-  return tg_host::launch_gated_attention_bwd(Q, K, V, g, O, dO, lse, cu_kept, B, M_capacity, max_seqlen,
+  return tg_host::launch_gated_attention_bwd(Q, K, V, g, H_g, O, dO, lse, cu_kept, B, M_capacity, max_seqlen,
                                              H_q, H_kv, d_h, tau, beta, dQ, dK, dV, dbias, status,
                                              S(stream));
 }
 
-tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float *g_kept, int32_t H_g,
                              const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
                              int32_t capacity, int32_t H_q, int32_t T_total, float *ds,
                              tg_stream_t stream) {
@@ -196,23 +222,27 @@ tg_status tg_gate_score_grad(const float *dbias, const float *beta, const float 
   if (B < 1 || capacity < 0 || H_q < 1 || H_q > 128 || T_total < 0) return TG_ERR_INVALID_ARG;
   for (int h = 0; h < H_q; ++h)
     if (!std::isfinite(beta[h])) return TG_ERR_INVALID_ARG;
-  return tg_host::launch_gate_score_grad(dbias, beta, g_kept, kept_idx, cu_kept, B, capacity, H_q, T_total, ds,
+  const tg_status st = check_gate_heads(H_g, H_q);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gate_score_grad(dbias, beta, g_kept, H_g, kept_idx, cu_kept, B, capacity, H_q, T_total, ds,
                                          S(stream));
 }
 
-tg_status tg_normalize_scores(const float *s, const uint8_t *instr_mask, const int32_t *cu_seqlens,
-                              int32_t B, int32_t T_total, float eps, float *b_out, int32_t *status,
+tg_status tg_normalize_scores(const float *s, int32_t H_g, const uint8_t *instr_mask, const int32_t *cu_seqlens,
+                              int32_t B, int32_t T_total, float eps, float *b_out, float *b_sel, int32_t *status,
                               tg_stream_t stream) {
   if (!s || !cu_seqlens || !b_out) return TG_ERR_INVALID_ARG;
   if (B < 1 || T_total < 0 || !std::isfinite(eps) || eps < 0.0f) return TG_ERR_INVALID_ARG;
+  const tg_status st = check_gate_heads(H_g, 0);
+  if (st != TG_OK) return st;
   if (B > kMaxSelectB) return TG_ERR_UNSUPPORTED;
   if (T_total == 0) return TG_OK;
-  return tg_host::launch_normalize_scores(s, instr_mask, cu_seqlens, B, T_total, eps, b_out, status,
+  return tg_host::launch_normalize_scores(s, H_g, instr_mask, cu_seqlens, B, T_total, eps, b_out, b_sel, status,
                                           S(stream));
 }
 
 tg_status tg_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                 const float *b, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
                                  int32_t B, int32_t M_capacity, int32_t max_seqlen, int32_t H_q,
                                  int32_t H_kv, int32_t d_h, const float *gain, const float *temp,
                                  uint16_t *O, int32_t *status, tg_stream_t stream) {
@@ -225,7 +255,9 @@ tg_status tg_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uin
     if (!std::isfinite(temp[h]) || temp[h] < 0.0f) return TG_ERR_INVALID_ARG;
   }
   if (H_q % H_kv != 0 || H_q > 128 || (d_h != 128 && d_h != 64)) return TG_ERR_UNSUPPORTED;
-  return tg_host::launch_gated_attention_eq8(Q, K, V, b, pos, cu_kept, B, M_capacity, max_seqlen, H_q,
+  const tg_status st = check_gate_heads(H_g, H_q);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gated_attention_eq8(Q, K, V, b, H_g, pos, cu_kept, B, M_capacity, max_seqlen, H_q,
                                              H_kv, d_h, gain, temp, O, status, S(stream));
 }
 
@@ -248,8 +280,34 @@ tg_status tg_gate_prune_layer(const uint16_t *h, const int32_t *pos, const uint8
   st = tg_host::launch_topk_select(s_out, instr_mask, cu_seqlens, B, T_total, K, kept_idx,
                                    capacity, cu_kept, status, S(stream));
   if (st != TG_OK) return st;
-  return tg_host::launch_gather(h, pos, g_out, cu_seqlens, B, T_total, d, kept_idx, cu_kept,
+  return tg_host::launch_gather(h, pos, g_out, 1, cu_seqlens, B, T_total, d, kept_idx, cu_kept,
                                 capacity, h_kept, pos_kept, g_kept, status, S(stream));
+}
+
+tg_status tg_gate_prune_layer_heads(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
+                                    const int32_t *cu_seqlens, int32_t B, int32_t T_total, int32_t d,
+                                    const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
+                                    int32_t d_g, int32_t H_g, int32_t K, float *s_heads, float *g_heads,
+                                    float *s_sel, int32_t *kept_idx, int32_t capacity, int32_t *cu_kept,
+                                    uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
+                                    tg_stream_t stream) {
+  tg_status st = check_gate_score(h, T_total, d, W1, W2, d_g, s_heads, 0.0f);
+  if (st == TG_OK) st = check_gate_heads(H_g, 0);
+  if (st == TG_OK && (!g_heads || !s_sel)) st = TG_ERR_INVALID_ARG;
+  if (st == TG_OK) st = check_select(s_sel, cu_seqlens, B, T_total, K, kept_idx, capacity, cu_kept);
+  if (st == TG_OK)
+    st = check_gather(h, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity, h_kept);
+  for (int c = 0; st == TG_OK && b2 && c < H_g; ++c)
+    if (!std::isfinite(b2[c])) st = TG_ERR_INVALID_ARG;
+  if (st != TG_OK) return st;
+  st = tg_host::launch_gate_score(h, T_total, d, instr_mask, W1, b1, W2, b2 ? b2[0] : 0.0f, d_g, s_heads,
+                                  g_heads, status, S(stream), false, 0.0f, H_g, b2, s_sel);
+  if (st != TG_OK) return st;
+  st = tg_host::launch_topk_select(s_sel, instr_mask, cu_seqlens, B, T_total, K, kept_idx, capacity, cu_kept,
+                                   status, S(stream));
+  if (st != TG_OK) return st;
+  return tg_host::launch_gather(h, pos, g_heads, H_g, cu_seqlens, B, T_total, d, kept_idx, cu_kept, capacity,
+                                h_kept, pos_kept, g_kept, status, S(stream));
 }
 
 tg_status tg_two_budget_prune_layer(const uint16_t *h, const int32_t *pos, const uint8_t *instr_mask,
@@ -275,7 +333,7 @@ tg_status tg_two_budget_prune_layer(const uint16_t *h, const int32_t *pos, const
   st = tg_host::launch_topk_select(s_out, instr_mask, cu_seqlens, B, T_total, K_prune, kept_idx + T_total,
                                    capacity - T_total, cu_packed + B, status, S(stream), T_total);
   if (st != TG_OK) return st;
-  return tg_host::launch_gather(h, pos, g_out, cu_seqlens, B, T_total, d, kept_idx, cu_packed, capacity,
+  return tg_host::launch_gather(h, pos, g_out, 1, cu_seqlens, B, T_total, d, kept_idx, cu_packed, capacity,
                                 h_kept, pos_kept, g_kept, status, S(stream), 2 * B);
 }
 

@@ -14,7 +14,9 @@
 //   warp 0       TMA producer: Q tiles once, then the K/V ring (kStages deep)
 //   warp 1       tensor-memory owner and MMA issuer:  S_t = Q_t K^T ; O_t += P_t V
 //   warp 2       bias producer: beta_h * log2(g_j) of each K/V tile's 128 keys, both heads,
-//                into a shared-memory ring that follows the K/V stages
+//                into a shared-memory ring that follows the K/V stages. The gate may be per
+//                head (section 3.4: a per-head bias): g is [M, H_g] and query head h reads
+//                gate head h / (H_q / H_g)
 //   warps 4-7    softmax + correction + epilogue for Q tile 0 (thread = query row = TMEM lane)
 //   warps 8-11   the same for Q tile 1
 // Online softmax with a lazily updated running max: the reference max m only moves when the
@@ -55,6 +57,7 @@ enum { kLogGate = 0, kEq8 = 1 };
 
 struct AttnParams {
   const float *g;            // kLogGate: gate values g_j; kEq8: normalised scores b_j (or NULL)
+  int32_t g_cols, g_group;   // gate heads per row (H_g); query heads per gate head (H_q / H_g)
   const int32_t *pos;        // kEq8: original position ids of the kept rows
   const int32_t *cu_kept;
   int32_t B, M_cap, max_seqlen, H_q, H_kv, group, heads_per_cta, pairs, n_qt_max;
@@ -315,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.g != nullptr) {
       const float beta0 = p.beta[h0];
       const float beta1 = n_tiles > 1 ? p.beta[h0 + 1] : 0.0f;
+      // per-head gates: query head h reads gate head h / g_group of its key's row
+      const int col0 = h0 / p.g_group;
+      const int col1 = n_tiles > 1 ? (h0 + 1) / p.g_group : col0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
@@ -325,19 +331,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         float *dst = sBias + st * 256;
-        float gv[4];
+        float gv0[4], gv1[4];
+        const float pad = MODE == kEq8 ? 0.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int k = j * kBlockN + lane * 4 + i;
-          gv[i] = k < seq_len ? p.g[seq_start + k] : (MODE == kEq8 ? 0.0f : 1.0f);
+          const size_t row = static_cast<size_t>(seq_start + k) * p.g_cols;
+          gv0[i] = k < seq_len ? p.g[row + col0] : pad;
+          gv1[i] = col1 == col0 ? gv0[i] : (k < seq_len ? p.g[row + col1] : pad);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           // kLogGate: beta_h log2(g_j) (beta = 0 means g^0 = 1, a zero bias even where g = 0);
           // kEq8: gain_h log2(e) b_j, the log2-unit score bias before the row's temperature
-          const float v = MODE == kEq8 ? gv[i] : lg2(gv[i]);
-          dst[lane * 4 + i] = beta0 == 0.0f ? 0.0f : beta0 * v;
-          dst[128 + lane * 4 + i] = beta1 == 0.0f ? 0.0f : beta1 * v;
+          const float v0 = MODE == kEq8 ? gv0[i] : lg2(gv0[i]);
+          const float v1 = col1 == col0 ? v0 : (MODE == kEq8 ? gv1[i] : lg2(gv1[i]));
+          dst[lane * 4 + i] = beta0 == 0.0f ? 0.0f : beta0 * v0;
+          dst[128 + lane * 4 + i] = beta1 == 0.0f ? 0.0f : beta1 * v1;
         }
         tg::mbar_arrive(&bias_full[st]);
       }
@@ -570,12 +580,14 @@ namespace tg_host {
 
 namespace {
 
-AttnParams common_params(const float *bias_src, const int32_t *pos, const int32_t *cu_kept, int32_t B,
-                         int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv, uint16_t *O,
+AttnParams common_params(const float *bias_src, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
+                         int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv, uint16_t *O,
                          int32_t *status) {
   AttnParams p;
   p.lse = nullptr;
   p.g = bias_src;
+  p.g_cols = H_g;
+  p.g_group = H_q / H_g;
   p.pos = pos;
   p.cu_kept = cu_kept;
   p.B = B;
@@ -598,12 +610,12 @@ AttnParams common_params(const float *bias_src, const int32_t *pos, const int32_
 }  // namespace
 
 tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                 const float *g, const int32_t *cu_kept, int32_t B,
+                                 const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
                                  int32_t *status, cudaStream_t stream, float *lse) {
   if (M_cap == 0 || max_seqlen == 0) return TG_OK;
-  AttnParams p = common_params(g, nullptr, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
+  AttnParams p = common_params(g, H_g, nullptr, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
   p.lse = lse;
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
@@ -616,13 +628,13 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
 }
 
 tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                     const float *b, const int32_t *pos, const int32_t *cu_kept,
+                                     const float *b, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
                                      int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q,
                                      int32_t H_kv, int32_t d_h, const float *gain,
                                      const float *temp, uint16_t *O, int32_t *status,
                                      cudaStream_t stream) {
   if (M_cap == 0 || max_seqlen == 0) return TG_OK;
-  AttnParams p = common_params(b, pos, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
+  AttnParams p = common_params(b, H_g, pos, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale_log2[h] = h < H_q ? temp[h] : 0.0f;

@@ -24,6 +24,7 @@ constexpr int kMaxHeads = 128;
 struct BwdParams {
   const uint16_t *Q, *K, *V, *O, *dO;
   const float *g;
+  int32_t g_cols, g_group;  // gate heads per row (H_g); query heads per gate head
   const float *lse;
   const int32_t *cu_kept;
   int32_t B, M_cap, H_q, H_kv, group, n_tiles;
@@ -135,7 +136,8 @@ template <int D>
 __device__ __forceinline__ void key_bias(BwdSmem<D> &sm, const BwdParams &p, int row0, int nk, int h) {
   for (int c = threadIdx.x; c < kT; c += kThreads) {
     float b = 0.0f;
-    if (p.g != nullptr && p.beta[h] != 0.0f && c < nk) b = p.beta[h] * logf(p.g[row0 + c]);
+    if (p.g != nullptr && p.beta[h] != 0.0f && c < nk)
+      b = p.beta[h] * logf(p.g[static_cast<size_t>(row0 + c) * p.g_cols + h / p.g_group]);
     sm.bias[c] = b;
   }
 }
@@ -265,11 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   }
 }
 
-// ---- the gate-score gradient: ds[kept_idx[m]] = (1 - g_m) sum_h beta_h dbias[m, h] ----
+// ---- the gate-score gradient: ds[kept_idx[m], c] = (1 - g[m, c]) sum over the query heads h
+// that read gate head c of beta_h dbias[m, h] (one gate head: every h) ----
 struct ScoreGradParams {
   const float *dbias, *g_kept;
   const int32_t *kept_idx, *cu_kept;
-  int32_t B, capacity, H_q, T;
+  int32_t B, capacity, H_q, H_g, T;
   float *ds;
   float beta[kMaxHeads];
 };
@@ -278,11 +281,15 @@ __global__ void __launch_bounds__(256) gate_score_grad_kernel(const __grid_const
   tg::pdl_wait();
   tg::pdl_launch_dependents();
   const int M = max(0, min(p.cu_kept[p.B], p.capacity));
-  for (int m = blockIdx.x * 256 + threadIdx.x; m < M; m += gridDim.x * 256) {
+  const int per = p.H_q / p.H_g;
+  const long long n = static_cast<long long>(M) * p.H_g;
+  for (long long e = blockIdx.x * 256LL + threadIdx.x; e < n; e += gridDim.x * 256LL) {
+    const int m = static_cast<int>(e / p.H_g), c = static_cast<int>(e % p.H_g);
     float acc = 0.0f;
-    for (int h = 0; h < p.H_q; ++h) acc = fmaf(p.beta[h], p.dbias[static_cast<size_t>(m) * p.H_q + h], acc);
+    for (int h = c * per; h < (c + 1) * per; ++h)
+      acc = fmaf(p.beta[h], p.dbias[static_cast<size_t>(m) * p.H_q + h], acc);
     const int j = p.kept_idx[m];
-    if (j >= 0 && j < p.T) p.ds[j] = acc * (1.0f - p.g_kept[m]);
+    if (j >= 0 && j < p.T) p.ds[static_cast<size_t>(j) * p.H_g + c] = acc * (1.0f - p.g_kept[e]);
   }
 }
 
@@ -307,7 +314,7 @@ tg_status launch_bwd_d(const BwdParams &p, int n_tiles, cudaStream_t stream) {
 namespace tg_host {
 
 tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                                     const float *g, const uint16_t *O, const uint16_t *dO,
+                                     const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,
                                      const float *lse, const int32_t *cu_kept, int32_t B, int32_t M_cap,
                                      int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h,
                                      const float *tau, const float *beta, float *dQ, float *dK, float *dV,
@@ -320,6 +327,8 @@ tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const
   p.O = O;
   p.dO = dO;
   p.g = g;
+  p.g_cols = H_g;
+  p.g_group = H_q / H_g;
   p.lse = lse;
   p.cu_kept = cu_kept;
   p.B = B;
@@ -343,7 +352,7 @@ tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const
   return TG_ERR_UNSUPPORTED;
 }
 
-tg_status launch_gate_score_grad(const float *dbias, const float *beta, const float *g_kept,
+tg_status launch_gate_score_grad(const float *dbias, const float *beta, const float *g_kept, int32_t H_g,
                                  const int32_t *kept_idx, const int32_t *cu_kept, int32_t B,
                                  int32_t capacity, int32_t H_q, int32_t T, float *ds, cudaStream_t stream) {
   if (capacity == 0) return TG_OK;
@@ -355,10 +364,11 @@ tg_status launch_gate_score_grad(const float *dbias, const float *beta, const fl
   p.B = B;
   p.capacity = capacity;
   p.H_q = H_q;
+  p.H_g = H_g;
   p.T = T;
   p.ds = ds;
   for (int h = 0; h < kMaxHeads; ++h) p.beta[h] = h < H_q ? beta[h] : 0.0f;
-  int grid = (capacity + 255) / 256;
+  int grid = static_cast<int>((static_cast<long long>(capacity) * H_g + 255) / 256);
   if (grid > num_sms() * 4) grid = num_sms() * 4;
   return record_cuda(launch_pdl(gate_score_grad_kernel, dim3(grid), dim3(256), 0, stream, p));
 }

@@ -1,7 +1,7 @@
 // tg_gather.cu — slice the kept rows (TokenGate deep dive, section 3.4: hidden_states[:, keep]
 // and position_ids[:, keep], the original position ids) and carry each kept token's gate
-// value with it (TokenGate paper page, Figure 1 (b)); plus RoPE at the gathered original
-// positions.
+// value (or its H_g per-head gate values, section 3.4) with it (TokenGate paper page,
+// Figure 1 (b)); plus RoPE at the gathered original positions.
 //
 // Gather: one warp per kept row, 16-byte vector loads and streaming stores; the grid is a
 // fixed multiple of the SM count and strides over rows, so it needs no host knowledge of
@@ -17,6 +17,7 @@ struct GatherParams {
   const uint16_t *h;
   const int32_t *pos;
   const float *g;
+  int32_t H_g;  // gate values per row (per-head gates: H_g <= 32, one lane each)
   const int32_t *cu_seqlens;
   int32_t B, T, d;
   int32_t B_kept;  // cu_kept has B_kept + 1 entries (B for one list; 2B for a two-budget pack)
@@ -88,8 +89,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
         }
         p.pos_kept[m] = pv;
       }
-      if (p.g_kept && p.g) p.g_kept[m] = p.g[j];
     }
+    if (p.g_kept && p.g && lane < p.H_g)
+      p.g_kept[static_cast<size_t>(m) * p.H_g + lane] = p.g[static_cast<size_t>(j) * p.H_g + lane];
   }
 }
 
@@ -155,18 +157,16 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
 
 namespace tg_host {
 
-tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g,
+tg_status launch_gather(const uint16_t *h, const int32_t *pos, const float *g, int32_t H_g,
                         const int32_t *cu_seqlens, int32_t B, int32_t T, int32_t d,
                         const int32_t *kept_idx, const int32_t *cu_kept, int32_t capacity,
                         uint16_t *h_kept, int32_t *pos_kept, float *g_kept, int32_t *status,
                         cudaStream_t stream, int32_t B_kept) {
   if (capacity == 0) return TG_OK;
-  GatherParams p{h, pos, g, cu_seqlens, B, T, d, B_kept < 0 ? B : B_kept, kept_idx, cu_kept, capacity,
+  GatherParams p{h, pos, g, H_g, cu_seqlens, B, T, d, B_kept < 0 ? B : B_kept, kept_idx, cu_kept, capacity,
                  h_kept, pos_kept, g_kept, status};
-  const int rows_per_wave = num_sms() * 8 * kGatherWarps;
   int grid = (capacity + kGatherWarps - 1) / kGatherWarps;
   if (grid > num_sms() * 8) grid = num_sms() * 8;
-  (void)rows_per_wave;
   return record_cuda(launch_pdl(gather_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, p));
 }
 

@@ -83,7 +83,7 @@ tg_status record_cuda(cudaError_t e) {
 
 extern "C" {
 
-int32_t tg_version(void) { return 100; }
+int32_t tg_version(void) { return 200; }
 
 const char *tg_status_string(tg_status s) {
   switch (s) {

@@ -31,16 +31,20 @@ constexpr int kMaxDg = 512;
 constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
 constexpr int kPair = 2;  // CTAs of a cluster: neighbouring row tiles that share each W1 stage
+constexpr int kMaxGateHeads = 16;
 
 struct ScoreParams {
   int32_t T, d, d_g, n_items, item_n, n_tiles, KT;
   float ln_eps;  // fused RMSNorm (LN_2 of the residual): 1 / sqrt(mean(h^2) + ln_eps) per row
   const float *b1;
-  const uint16_t *w2;
+  const uint16_t *w2;  // [H_g, d_g] (one row per gate head)
   float b2;
+  int32_t H_g;                  // gate heads (section 3.4: a per-head bias), <= kMaxGateHeads
+  float b2h[kMaxGateHeads];     // per-head second-layer bias (H_g > 1)
   const uint8_t *mask;
-  float *s_out;
-  float *g_out;
+  float *s_out;  // [T, H_g]
+  float *g_out;  // [T, H_g] or NULL
+  float *s_sel;  // H_g > 1: [T] uniform head aggregation (the row mean) that top-K ranks
   int32_t *status;
   uint64_t wait_limit, drain_limit;
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
@@ -50,13 +54,15 @@ struct SmemLayout {
   uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_rms, off_bar, total;
 };
 
-__host__ __device__ inline SmemLayout score_smem_layout(int item_n) {
+// ghp: gate heads padded to 1, 2, 4, 8 or 16. One head keeps w2 as fp32 [d_g]; more heads keep
+// W2 as bf16 pairs [d_g][ghp / 2] (16 KB at 16 heads), zero past H_g.
+__host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   SmemLayout L;
   L.a_bytes = kBM * kBK * 2;                               // 16 KB
   L.b_bytes = static_cast<uint32_t>(item_n) * kBK * 2;     // <= 32 KB, a multiple of 1 KB
   L.off_b = kStages * L.a_bytes;
   L.off_w2 = L.off_b + kStages * L.b_bytes;
-  L.off_b1 = L.off_w2 + kMaxDg * 4;
+  L.off_b1 = L.off_w2 + (ghp == 1 ? kMaxDg * 4 : kMaxDg * ghp * 2);
   L.off_rms = L.off_b1 + kMaxDg * 4;           // [2 tiles][128 rows] fp32 1 / rms
   L.off_bar = L.off_rms + 2 * kBM * 4;
   L.total = L.off_bar + 256 + 1024;  // barriers + slots, plus alignment slack
@@ -90,17 +96,18 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <bool NORM>
+template <bool NORM, int GHP>
 __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = score_smem_layout(p.item_n);
+  const SmemLayout L = score_smem_layout(p.item_n, GHP);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
   float *s_w2 = reinterpret_cast<float *>(smem + L.off_w2);
+  uint32_t *s_w2h = reinterpret_cast<uint32_t *>(smem + L.off_w2);  // GHP > 1: [d_g][GHP / 2] bf16 pairs
   float *s_b1 = reinterpret_cast<float *>(smem + L.off_b1);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
   uint64_t *empty = full + kStages;
@@ -147,7 +154,16 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   tg::pdl_wait();
   tg::pdl_launch_dependents();
   for (int i = threadIdx.x; i < p.d_g; i += blockDim.x) {
-    s_w2[i] = tg::bf16_bits_to_float(p.w2[i]);
+    if (GHP == 1) {
+      s_w2[i] = tg::bf16_bits_to_float(p.w2[i]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < GHP / 2; ++k) {
+        const uint32_t lo = 2 * k < p.H_g ? p.w2[static_cast<size_t>(2 * k) * p.d_g + i] : 0u;
+        const uint32_t hi = 2 * k + 1 < p.H_g ? p.w2[static_cast<size_t>(2 * k + 1) * p.d_g + i] : 0u;
+        s_w2h[i * (GHP / 2) + k] = lo | (hi << 16);
+      }
+    }
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
   tg::tc_fence_before();
@@ -243,7 +259,9 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     bool ok = true;
     for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride, ++ti) {
       const int tile = pr * kPair + static_cast<int>(rank);
-      float acc = 0.0f;
+      float acc[GHP];
+#pragma unroll
+      for (int c = 0; c < GHP; ++c) acc[c] = 0.0f;
       float inv_rms = 1.0f;
       if (NORM) {
         ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&rms_ready[ti & 1], (ti >> 1) & 1, vabort, p.wait_limit));
@@ -267,7 +285,28 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
             const float u = NORM ? fmaf(__uint_as_float(v[i]), inv_rms, s_b1[hid0 + c0 + i])
                                  : __uint_as_float(v[i]) + s_b1[hid0 + c0 + i];
             const float silu = __fdividef(u, 1.0f + __expf(-u));
-            acc = fmaf(s_w2[hid0 + c0 + i], silu, acc);
+            if constexpr (GHP == 1) {
+              acc[0] = fmaf(s_w2[hid0 + c0 + i], silu, acc[0]);
+            } else {
+              // every thread reads the same column's weights: a shared-memory broadcast
+              uint32_t w[GHP / 2];
+              const uint32_t *src = s_w2h + (hid0 + c0 + i) * (GHP / 2);
+              if constexpr (GHP >= 8) {
+#pragma unroll
+                for (int k = 0; k < GHP / 2; k += 4) {
+                  const uint4 q = *reinterpret_cast<const uint4 *>(src + k);
+                  w[k] = q.x; w[k + 1] = q.y; w[k + 2] = q.z; w[k + 3] = q.w;
+                }
+              } else {
+#pragma unroll
+                for (int k = 0; k < GHP / 2; ++k) w[k] = src[k];
+              }
+#pragma unroll
+              for (int k = 0; k < GHP / 2; ++k) {
+                acc[2 * k] = fmaf(__uint_as_float(w[k] << 16), silu, acc[2 * k]);
+                acc[2 * k + 1] = fmaf(__uint_as_float(w[k] & 0xFFFF0000u), silu, acc[2 * k + 1]);
+              }
+            }
           }
         }
         tg::tc_fence_before();
@@ -281,11 +320,26 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       }
       const int row = tile * kBM + r;
       if (row < p.T) {
-        const float s = acc + p.b2;
-        p.s_out[row] = s;
-        if (p.g_out) {
-          const bool keep_always = p.mask && p.mask[row];
-          p.g_out[row] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
+        const bool keep_always = p.mask && p.mask[row];
+        if (GHP == 1) {
+          const float s = acc[0] + p.b2;
+          p.s_out[row] = s;
+          if (p.s_sel != nullptr && p.s_sel != p.s_out) p.s_sel[row] = s;  // one head: the mean is s
+          if (p.g_out) p.g_out[row] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
+        } else {
+          // per-head scores and gates, and their uniform aggregation (head order, then / H_g)
+          float sum = 0.0f;
+          const size_t base = static_cast<size_t>(row) * p.H_g;
+#pragma unroll
+          for (int c = 0; c < GHP; ++c) {
+            if (c < p.H_g) {
+              const float s = acc[c] + p.b2h[c];
+              sum += s;
+              p.s_out[base + c] = s;
+              if (p.g_out) p.g_out[base + c] = keep_always ? 1.0f : 1.0f / (1.0f + __expf(-s));
+            }
+          }
+          p.s_sel[row] = sum / static_cast<float>(p.H_g);
         }
       }
     }
@@ -357,12 +411,33 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
 
 namespace tg_host {
 
+namespace {
+
+template <bool NORM>
+decltype(&gate_score_kernel<NORM, 1>) score_kernel_for(int ghp) {
+  switch (ghp) {
+    case 1: return gate_score_kernel<NORM, 1>;
+    case 2: return gate_score_kernel<NORM, 2>;
+    case 4: return gate_score_kernel<NORM, 4>;
+    case 8: return gate_score_kernel<NORM, 8>;
+    default: return gate_score_kernel<NORM, 16>;
+  }
+}
+
+}  // namespace
+
 tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8_t *mask,
                             const uint16_t *W1, const float *b1, const uint16_t *w2, float b2,
                             int32_t d_g, float *s_out, float *g_out, int32_t *status,
-                            cudaStream_t stream, bool rmsnorm, float ln_eps) {
+                            cudaStream_t stream, bool rmsnorm, float ln_eps, int32_t H_g,
+                            const float *b2h, float *s_sel) {
   if (T == 0) return TG_OK;
+  if (H_g < 1 || H_g > kMaxGateHeads) return TG_ERR_UNSUPPORTED;
   ScoreParams p;
+  p.H_g = H_g;
+  for (int c = 0; c < kMaxGateHeads; ++c) p.b2h[c] = (b2h != nullptr && c < H_g) ? b2h[c] : 0.0f;
+  p.s_sel = s_sel;
+  const int ghp = H_g == 1 ? 1 : H_g <= 2 ? 2 : H_g <= 4 ? 4 : H_g <= 8 ? 8 : 16;
   p.T = T;
   p.d = d;
   p.d_g = d_g;
@@ -397,11 +472,11 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
     if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
-  const SmemLayout L = score_smem_layout(p.item_n);
+  const SmemLayout L = score_smem_layout(p.item_n, ghp);
   const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
   int pairs = num_sms() / kPair;
   if (pairs > n_pairs) pairs = n_pairs;
-  auto kernel = rmsnorm ? gate_score_kernel<true> : gate_score_kernel<false>;
+  auto kernel = rmsnorm ? score_kernel_for<true>(ghp) : score_kernel_for<false>(ghp);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
   return record_cuda(launch_pdl(kernel, dim3(pairs * kPair), dim3(rmsnorm ? kThreadsNorm : kThreads),

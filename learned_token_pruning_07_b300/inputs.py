@@ -123,6 +123,7 @@ def with_changes(wl: Workload, **kw) -> Workload:
 
 _TAG_H, _TAG_W1, _TAG_W2, _TAG_HEAVY, _TAG_MASK, _TAG_TAU, _TAG_BETA = 11, 12, 13, 14, 15, 16, 17
 _TAG_S, _TAG_Q, _TAG_K, _TAG_V, _TAG_G = 21, 22, 23, 24, 25
+_TAG_W2H, _TAG_B2H, _TAG_GH = 31, 32, 33
 
 
 def _rng(seed: int, tag: int, extra: int = 0) -> np.random.Generator:
@@ -188,6 +189,20 @@ def make_gate_inputs(wl: Workload) -> dict:
         "cu_seqlens": cu_seqlens_of(wl.seq_lens),
         "pos": make_positions(wl),
     }
+
+
+def make_gate_head_weights(wl: Workload, H_g: int) -> dict:
+    """Second score layer with one row per gate head: W2 [H_g, d_g] ~ N(0, 1/d_g) in bf16 and a
+    per-head bias b2 [H_g] ~ N(0, 0.1^2) in fp32."""
+    W2 = _rng(wl.seed, _TAG_W2H, H_g).standard_normal((H_g, wl.d_g), dtype=np.float32)
+    W2 *= np.float32(1.0 / np.sqrt(wl.d_g))
+    b2 = (_rng(wl.seed, _TAG_B2H, H_g).standard_normal(H_g, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    return {"W2": f32_to_bf16_bits(W2), "b2": b2}
+
+
+def make_head_gates(wl: Workload, M: int, H_g: int, tag_extra: int = 0) -> np.ndarray:
+    """Per-head gate values of M kept rows, g ~ U(0.02, 1) fp32 [M, H_g]."""
+    return _rng(wl.seed, _TAG_GH, 100 * H_g + tag_extra).uniform(0.02, 1.0, (M, H_g)).astype(np.float32)
 
 
 def quantise_levels(s: np.ndarray, instr_mask: np.ndarray, cu_seqlens: np.ndarray,

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.tg_version() == 100
+    assert lib.tg_version() == 200
     assert lib.tg_status_string(binding.TG_OK) == b"ok"
     assert b"capacity" in lib.tg_status_string(binding.TG_ERR_CAPACITY)
 
@@ -61,8 +61,10 @@ def test_select_rejects_bad_arguments(lib):
 
 def test_gather_rejects_bad_arguments(lib):
     f = lib.tg_gather_kept
-    assert f(FAKE, None, None, FAKE, 1, 10, 12, FAKE, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
-    assert f(FAKE, None, None, FAKE, 1, 10, 16, None, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, None, 1, FAKE, 1, 10, 12, FAKE, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, None, 1, FAKE, 1, 10, 16, None, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, None, 0, FAKE, 1, 10, 16, FAKE, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(FAKE, None, None, 17, FAKE, 1, 10, 16, FAKE, FAKE, 10, FAKE, None, None, None, None) == binding.TG_ERR_UNSUPPORTED
 
 
 def test_attention_rejects_bad_arguments(lib):
@@ -71,12 +73,14 @@ def test_attention_rejects_bad_arguments(lib):
     beta = np.ones(4, np.float32)
     bad_tau = np.array([1, 0, 1, 1], np.float32)
     neg_beta = np.array([1, -1, 1, 1], np.float32)
-    args = lambda t, b, hq=4, hkv=2, dh=64: (FAKE, FAKE, FAKE, None, FAKE, 1, 64, 64, hq, hkv, dh,
-                                             t.ctypes.data, b.ctypes.data, FAKE, None, None)
+    args = lambda t, b, hq=4, hkv=2, dh=64, hg=1: (FAKE, FAKE, FAKE, None, hg, FAKE, 1, 64, 64, hq, hkv, dh,
+                                                   t.ctypes.data, b.ctypes.data, FAKE, None, None)
     assert f(*args(bad_tau, beta)) == binding.TG_ERR_INVALID_ARG
     assert f(*args(tau, neg_beta)) == binding.TG_ERR_INVALID_ARG
     assert f(*args(tau, beta, hq=4, hkv=3)) == binding.TG_ERR_UNSUPPORTED
     assert f(*args(tau, beta, dh=96)) == binding.TG_ERR_UNSUPPORTED
+    assert f(*args(tau, beta, hg=0)) == binding.TG_ERR_INVALID_ARG       # gate heads >= 1
+    assert f(*args(tau, beta, hg=3)) == binding.TG_ERR_UNSUPPORTED       # H_q % H_g != 0
 
 
 def test_rope_rejects_bad_arguments(lib):
@@ -99,11 +103,14 @@ def test_test_withhold_hook_validates_its_mask(lib):
 
 def test_normalize_scores_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(16)
-    assert lib.tg_normalize_scores(None, None, p, 1, 8, 1e-6, p, None, None) == binding.TG_ERR_INVALID_ARG
-    assert lib.tg_normalize_scores(p, None, p, 0, 8, 1e-6, p, None, None) == binding.TG_ERR_INVALID_ARG
-    assert lib.tg_normalize_scores(p, None, p, 1, 8, -1.0, p, None, None) == binding.TG_ERR_INVALID_ARG
-    assert lib.tg_normalize_scores(p, None, p, 1, 8, float("nan"), p, None, None) == binding.TG_ERR_INVALID_ARG
-    assert lib.tg_normalize_scores(p, None, p, 2000, 8, 1e-6, p, None, None) == binding.TG_ERR_UNSUPPORTED
+    f = lib.tg_normalize_scores
+    assert f(None, 1, None, p, 1, 8, 1e-6, p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(p, 1, None, p, 0, 8, 1e-6, p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(p, 1, None, p, 1, 8, -1.0, p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(p, 1, None, p, 1, 8, float("nan"), p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(p, 1, None, p, 2000, 8, 1e-6, p, None, None, None) == binding.TG_ERR_UNSUPPORTED
+    assert f(p, 0, None, p, 1, 8, 1e-6, p, None, None, None) == binding.TG_ERR_INVALID_ARG
+    assert f(p, 32, None, p, 1, 8, 1e-6, p, None, None, None) == binding.TG_ERR_UNSUPPORTED
 
 
 def test_eq8_attention_rejects_bad_arguments(lib):
@@ -112,13 +119,14 @@ def test_eq8_attention_rejects_bad_arguments(lib):
     neg = ones.copy()
     neg[3] = -0.5
     f = lambda a: a.ctypes.data
-    call = lambda pos, gain, temp, hq=16, hkv=8, dh=128: lib.tg_gated_attention_eq8(
-        p, p, p, None, pos, p, 1, 100, 100, hq, hkv, dh, gain, temp, p, None, None)
+    call = lambda pos, gain, temp, hq=16, hkv=8, dh=128, hg=1: lib.tg_gated_attention_eq8(
+        p, p, p, None, hg, pos, p, 1, 100, 100, hq, hkv, dh, gain, temp, p, None, None)
     assert call(None, f(ones), f(ones)) == binding.TG_ERR_INVALID_ARG          # positions required
     assert call(p, f(neg), f(ones)) == binding.TG_ERR_INVALID_ARG              # gain >= 0
     assert call(p, f(ones), f(neg)) == binding.TG_ERR_INVALID_ARG              # temperature >= 0
     assert call(p, f(ones), f(ones), dh=96) == binding.TG_ERR_UNSUPPORTED
     assert call(p, f(ones), f(ones), hq=12, hkv=8) == binding.TG_ERR_UNSUPPORTED
+    assert call(p, f(ones), f(ones), hg=3) == binding.TG_ERR_UNSUPPORTED
 
 
 def test_rmsnorm_entry_points_reject_bad_arguments(lib):
@@ -127,3 +135,27 @@ def test_rmsnorm_entry_points_reject_bad_arguments(lib):
     assert lib.tg_gate_score_rmsnorm(p, 10, 64, None, p, None, p, 0.0, 33, 1e-6, p, None, None, None) == binding.TG_ERR_UNSUPPORTED
     assert lib.tg_fold_rmsnorm_weight(None, p, 4, 4, p, None) == binding.TG_ERR_INVALID_ARG
     assert lib.tg_fold_rmsnorm_weight(p, p, 0, 4, p, None) == binding.TG_ERR_INVALID_ARG
+
+
+def test_gate_score_heads_entry_points_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    b2 = np.zeros(4, np.float32)
+    bad_b2 = b2.copy()
+    bad_b2[2] = np.inf
+    f = lib.tg_gate_score_heads
+    call = lambda hg=4, rms=0, eps=1e-6, s_sel=p, b=b2: f(p, 128, 256, None, p, None, p, b.ctypes.data, 64, hg,
+                                                          rms, eps, p, None, s_sel, None, None)
+    assert call(hg=0) == binding.TG_ERR_INVALID_ARG
+    assert call(hg=17) == binding.TG_ERR_UNSUPPORTED
+    assert call(s_sel=None) == binding.TG_ERR_INVALID_ARG            # the head mean is required
+    assert call(rms=2) == binding.TG_ERR_INVALID_ARG
+    assert call(rms=1, eps=-1.0) == binding.TG_ERR_INVALID_ARG
+    assert call(b=bad_b2) == binding.TG_ERR_INVALID_ARG
+    g = lib.tg_gate_prune_layer_heads
+    assert g(p, None, None, p, 1, 128, 256, p, None, p, None, 64, 4, 8, p, None, p, p, 128, p, p, None, None,
+             None, None) == binding.TG_ERR_INVALID_ARG               # g_heads required
+    assert g(p, None, None, p, 1, 128, 256, p, None, p, None, 64, 4, -1, p, p, p, p, 128, p, p, None, None,
+             None, None) == binding.TG_ERR_INVALID_ARG               # K >= 0
+    s = lib.tg_gate_score_grad
+    beta = np.ones(4, np.float32)
+    assert s(p, beta.ctypes.data, p, 3, p, p, 1, 8, 4, 16, p, None) == binding.TG_ERR_UNSUPPORTED

@@ -91,9 +91,40 @@ def test_backward_tiny_dh64():
     _case(I.WORKLOADS["tiny"], [96, 33], seed=1)
 
 
-@pytest.mark.parametrize("lens", [[1], [63, 64, 65], [129, 2, 200]])
+@pytest.mark.parametrize("lens", [[1], [63, 64, 65], [129, 0, 2, 200], [700, 1030]])
 def test_backward_varlen_dh128(lens):
     _case(I.WORKLOADS["qwen3_1p7b_8k"], lens, seed=len(lens))
+
+
+def test_backward_mha_and_odd_group():
+    _case(I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=4, H_kv=4), [130, 70], seed=21)
+    _case(I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=6, H_kv=2), [130, 70], seed=22)
+
+
+def test_backward_is_deterministic():
+    # every output element is written once after a fixed-order sum: two runs agree bit for bit
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    lens = [300, 129]
+    cu = I.cu_seqlens_of(lens)
+    M = int(cu[-1])
+    at = I.make_attention_inputs(wl, M, tag_extra=31)
+    dO = I.f32_to_bf16_bits(np.random.default_rng(331).standard_normal((M, wl.H_q, wl.d_h)).astype(np.float32))
+    Qd, Kd, Vd, gd, cud, dOd = dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(at["g"]), dev(cu), dev(dO)
+    O_d = torch.zeros((M, wl.H_q, wl.d_h), dtype=torch.int16, device="cuda")
+    lse = torch.zeros((M, wl.H_q), dtype=torch.float32, device="cuda")
+    st = status_word()
+    tg.gated_attention_lse(Qd, Kd, Vd, cud, at["tau"], at["beta"], O_d, lse, max_seqlen=max(lens), g=gd, status=st)
+    runs = []
+    for _ in range(2):
+        out = [torch.zeros(sh, dtype=torch.float32, device="cuda")
+               for sh in ((M, wl.H_q, wl.d_h), (M, wl.H_kv, wl.d_h), (M, wl.H_kv, wl.d_h), (M, wl.H_q))]
+        tg.gated_attention_bwd(Qd, Kd, Vd, O_d, dOd, lse, cud, at["tau"], at["beta"], *out, max_seqlen=max(lens),
+                               g=gd, status=st)
+        runs.append([host(t) for t in out])
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    for a, b in zip(*runs):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
 def test_backward_without_gate_and_with_beta_zero():
