@@ -825,10 +825,11 @@ def run_gpu(args, rank, world, local):
                 del g2, p2
                 torch.cuda.empty_cache()
 
-    paper = paper_form(path, torch, flush, args.steps) if rank == 0 else None
-    twob = two_budget(path, torch, flush, args.steps) if rank == 0 else None
-    bwd = backward(path, torch, flush, args.steps) if rank == 0 else None
-    hds = heads(path, torch, flush, args.steps) if rank == 0 else None
+    extras = rank == 0 and args.extras
+    paper = paper_form(path, torch, flush, args.steps) if extras else None
+    twob = two_budget(path, torch, flush, args.steps) if extras else None
+    bwd = backward(path, torch, flush, args.steps) if extras else None
+    hds = heads(path, torch, flush, args.steps) if extras else None
     longctx = long_context(torch, flush, args.steps) if (args.long_context and rank == 0) else None
 
     cpu = None
@@ -888,6 +889,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--long-context", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the 128K workload: pruned step vs full causal attention")
+    ap.add_argument("--extras", action=argparse.BooleanOptionalAction, default=True,
+                    help="also measure the paper form, the two-budget pack, the backward and per-head gates")
     ap.add_argument("--oracle-frac", type=int, default=8)
     args = ap.parse_args(argv)
     if args.warmup < 3:
