@@ -12,7 +12,8 @@
 // packed bf16) and the output accumulators O_0, O_1 (fp32 128 x d_h).
 // Warp roles (12 warps):
 //   warp 0       TMA producer: Q tiles once, then the K/V ring (kStages deep)
-//   warp 1       tensor-memory owner and MMA issuer:  S_t = Q_t K^T ; O_t += P_t V
+//   warp 1       tensor-memory owner and MMA issuer:  S_t = Q_t K^T ; O_t += P_t V (the warp runs
+//                converged and one elected lane issues, which keeps the operands warp-uniform)
 //   warp 2       bias producer: beta_h * log2(g_j) of each K/V tile's 128 keys, both heads,
 //                into a shared-memory ring that follows the K/V stages. The gate may be per
 //                head (section 3.4: a per-head bias): g is [M, H_g] and query head h reads
@@ -231,13 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       *n_issued = issued;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    {
+      // ---------------- MMA issuer: the whole warp runs the loop, one elected lane issues ----------------
       const uint32_t idesc_s = tg::idesc_bf16_f32(kBlockM, kBlockN);        // Q K^T, both K-major
       const uint32_t idesc_o = tg::idesc_bf16_f32(kBlockM, D, 0, 1);        // P V, V MN-major
       const uint32_t colS[2] = {C::kColS0, C::kColS1};
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
-      bool ok = tg::mbar_wait(q_full, 0, vabort, p.wait_limit);
+      bool ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(q_full, 0, vabort, p.wait_limit));
       int consumed = 0;
       // descriptors of each operand buffer, built once; a K-step adds its byte offset / 16
       // (buffers of one kind are contiguous, so buffer i is the first one's descriptor + i * tile / 16)
@@ -251,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off16 = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
-          tg::mma_bf16_ss(dst, qd + off16, kd + off16, idesc_s, k != 0);
+          tg::mma_bf16_ss_elect(dst, qd + off16, kd + off16, idesc_s, k != 0);
         }
-        tg::mma_commit(&s_full[t]);
+        tg::mma_commit_elect(&s_full[t]);
       };
       auto issue_pv = [&](int t, int st, bool first) {
         const uint64_t vd = dv0 + st * kTile16;
@@ -261,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
           // keys 16k..16k+15: 16 rows of 128 B in every d-half; d-halves 16 KB apart
-          tg::mma_bf16_ts(dst, src + k * 8, vd + ((k * 2048) >> 4), idesc_o, !(first && k == 0));
+          tg::mma_bf16_ts_elect(dst, src + k * 8, vd + ((k * 2048) >> 4), idesc_o, !(first && k == 0));
         }
       };
       if (ok) {
-        if (!tg::mbar_wait(&kv_full[0], 0, vabort, p.wait_limit)) ok = false;
+        if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&kv_full[0], 0, vabort, p.wait_limit))) ok = false;
       }
       if (ok) {
         tg::tc_fence_after();
@@ -277,25 +278,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool has_next = j + 1 < n_kv;
           const int st_n = (j + 1) % C::kStages;
           for (int t = 0; t < n_tiles && ok; ++t) {
-            if (!tg::mbar_wait(&p_full[t], j & 1, vabort, p.wait_limit)) {
+            if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&p_full[t], j & 1, vabort, p.wait_limit))) {
               ok = false;
               break;
             }
             tg::tc_fence_after();
             issue_pv(t, st, j == 0);
-            tg::mma_commit(has_next ? &pv_done[t] : &o_final[t]);
+            tg::mma_commit_elect(has_next ? &pv_done[t] : &o_final[t]);
             if (t == n_tiles - 1) {
-              tg::mma_commit(&kv_empty[st]);
+              tg::mma_commit_elect(&kv_empty[st]);
               consumed = j + 1;
             }
             if (has_next) {
               if (t == 0 &&
-                  !tg::mbar_wait(&kv_full[st_n], ((j + 1) / C::kStages) & 1, vabort,
-                                 p.wait_limit)) {
+                  !__all_sync(0xFFFFFFFFu, tg::mbar_wait(&kv_full[st_n], ((j + 1) / C::kStages) & 1, vabort,
+                                                         p.wait_limit))) {
                 ok = false;
                 break;
               }
-              if (!tg::mbar_wait(&pv_done[t], j & 1, vabort, p.wait_limit)) {
+              if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&pv_done[t], j & 1, vabort, p.wait_limit))) {
                 ok = false;
                 break;
               }
@@ -305,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      *n_consumed = consumed;
+      if (lane == 0) *n_consumed = consumed;
       if (!ok) {
         *vabort = 1;
-        tg::mma_commit(drain);
+        tg::mma_commit_elect(drain);
         volatile int32_t never = 0;
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
