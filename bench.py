@@ -636,7 +636,7 @@ def backward(path, torch, flush, steps):
     torch.cuda.empty_cache()
     return {"forward_lse_us": f_us, "attention_bwd_us": b_us, "gate_score_grad_us": c_us,
             "attention_bwd_tflops": bwd_flops / (b_us * 1e-6) / 1e12,
-            "note": "fp32 CUDA-core backward (no tensor cores); single launches with events around each, "
+            "note": "tensor-core backward (row dots, dK/dV pass, dQ pass); single launches with events around each, "
                     "L2 flushed before each"}
 
 

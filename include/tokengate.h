@@ -220,8 +220,11 @@ TG_API tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, co
  *       beta_h ln g_j (so dL/d ln g_j = sum_h beta_h dbias[j, h]).
  *   O, dO [device] bf16 [M, H_q, d_h] (the forward's output and the incoming gradient);
  *   lse from tg_gated_attention_lse. Outputs are overwritten for rows < min(cu_kept[B], M_capacity).
- *   Deterministic (fixed-order sums, no atomics). This version computes on the CUDA cores in
- *   fp32 (64x64 tiles recomputed in shared memory). Other arguments as tg_gated_attention.
+ *   dQ also serves as the call's workspace: D_i = dO_i . o_i is kept in dQ[i, h, 0] until the
+ *   final pass writes dQ, so the library allocates nothing.
+ *   Compute: tcgen05 MMAs (bf16 operands, fp32 accumulation; P and c_h dX enter the products
+ *   rounded to bf16), fp32 elementwise. Deterministic (fixed-order sums, no atomics).
+ *   Other arguments as tg_gated_attention.
  */
 TG_API tg_status tg_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                                  const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,

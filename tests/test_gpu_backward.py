@@ -1,14 +1,18 @@
 """GPU parity: the backward of token-gated attention and the gate-score gradient, against the
 fp64 oracle (which is pinned to torch autograd and to finite differences).
 
-Like flash-attention backwards, the GPU forms D_i = dO_i . o_i from the forward's bf16 output
-O, whose elements carry a round-to-nearest error of at most 2^-9 relative, so
-|dD_i| <= 2^-9 sum_d |dO_id o_id|. dX = P (dP - D) is linear in D, so to first order the
-gradients move by at most
-    dQ_id: c_h dD_i sum_j P_ij |k_jd|        dK_jd: sum_h c_h sum_i P_ij dD_i |q_id|
-    dbias_jh: sum_i P_ij dD_i                dV: not at all
-(c_h = tau_h / sqrt(d_h)). The bar per element is that bound plus 1e-4 of the gradient's
-largest magnitude (fp32 sums and the fp32 log-sum-exp); log-sum-exp within 1e-3 absolute."""
+bf16 rounds to nearest with an 8-bit significand, so a rounded value is off by at most
+u = 2^-8 of itself. Two roundings move the GPU's gradients away from the exact ones:
+  * like flash-attention backwards, D_i = dO_i . o_i is formed from the forward's bf16 output,
+    so |dD_i| <= u sum_d |dO_id o_id|; dX = P (dP - D) is linear in D;
+  * the tensor-core products take P and c_h dX as bf16 operands (fp32 accumulation).
+To first order the gradients then move by at most, per element (c_h = tau_h / sqrt(d_h)):
+    dQ_id:    c_h dD_i sum_j P_ij |k_jd|  +  u c_h sum_j |dX_ij| |k_jd|
+    dK_jd:    sum_h [c_h sum_i P_ij dD_i |q_id|  +  u c_h sum_i |dX_ij| |q_id|]
+    dV_jd:    sum_h u sum_i P_ij |dO_id|
+    dbias_jh: sum_i P_ij dD_i                     (summed from fp32 P and dX)
+The bar per element is that bound plus 1e-4 of the gradient's largest magnitude (fp32 sums and
+the fp32 log-sum-exp); log-sum-exp within 1e-3 absolute."""
 import numpy as np
 import pytest
 import torch
@@ -49,7 +53,7 @@ def _case(wl, lens, seed, use_g=True, beta_zero=False):
     ref = O.gated_attention_bwd(Q64, K64, V64, g64, I.bf16_bits_to_f64(dO), cu, tau.astype(np.float64),
                                 beta.astype(np.float64))
     got = [host(t).astype(np.float64) for t in (dQ, dK, dV, dbias)]
-    bounds = _d_rounding_bounds(Q64, K64, V64, g64, I.bf16_bits_to_f64(dO), cu, tau, beta)
+    bounds = _rounding_bounds(Q64, K64, V64, g64, I.bf16_bits_to_f64(dO), cu, tau, beta)
     for name, a, b, bnd in zip(("dQ", "dK", "dV", "dbias"), got, ref, bounds):
         assert np.all(np.isfinite(a)), name
         tol = bnd + 1e-4 * float(np.max(np.abs(b))) + 1e-7
@@ -58,9 +62,13 @@ def _case(wl, lens, seed, use_g=True, beta_zero=False):
     return at, cu, g, tau, beta, ref, dbias
 
 
-def _d_rounding_bounds(Q, K, V, g, dO, cu, tau, beta):
-    """Per-element first-order bounds of the gradient change caused by forming D from a
-    bf16-rounded O (see the module docstring)."""
+U_BF16 = 2.0 ** -8
+
+
+def _rounding_bounds(Q, K, V, g, dO, cu, tau, beta):
+    """Per-element first-order bounds of the gradient change caused by the bf16 roundings of O
+    (inside D) and of the tensor-core operands P and c_h dX (see the module docstring). g is
+    [M] or [M, H_g] (query head h reads gate column h / (H_q / H_g))."""
     M, H_q, d_h = Q.shape
     group = H_q // K.shape[1]
     bq, bk, bv, bb = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V), np.zeros((M, H_q))
@@ -75,14 +83,19 @@ def _d_rounding_bounds(Q, K, V, g, dO, cu, tau, beta):
             c = float(tau[h]) / np.sqrt(d_h)
             x = c * (Q[a:e, h] @ K[a:e, kv].T)
             if g is not None and beta[h] != 0:
-                x = x + float(beta[h]) * np.log(g[a:e])[None, :]
+                gh = g[a:e] if g.ndim == 1 else g[a:e, h // (H_q // g.shape[1])]
+                x = x + float(beta[h]) * np.log(gh)[None, :]
             x = np.where(tri, x, -np.inf)
             P = np.exp(x - x.max(axis=1, keepdims=True))
             P /= P.sum(axis=1, keepdims=True)
             o = P @ V[a:e, kv]
-            dD = 2.0 ** -9 * np.sum(np.abs(dO[a:e, h] * o), axis=1)          # [n]
-            bq[a:e, h] = c * dD[:, None] * (P @ np.abs(K[a:e, kv]))
-            bk[a:e, kv] += c * (P * dD[:, None]).T @ np.abs(Q[a:e, h])
+            dP = dO[a:e, h] @ V[a:e, kv].T
+            dX = P * (dP - np.sum(dO[a:e, h] * o, axis=1, keepdims=True))
+            dD = U_BF16 * np.sum(np.abs(dO[a:e, h] * o), axis=1)          # [n]
+            aK, aQ = np.abs(K[a:e, kv]), np.abs(Q[a:e, h])
+            bq[a:e, h] = c * dD[:, None] * (P @ aK) + U_BF16 * c * (np.abs(dX) @ aK)
+            bk[a:e, kv] += c * (P * dD[:, None]).T @ aQ + U_BF16 * c * np.abs(dX).T @ aQ
+            bv[a:e, kv] += U_BF16 * P.T @ np.abs(dO[a:e, h])
             bb[a:e, h] = (P * dD[:, None]).sum(axis=0)
     return bq, bk, bv, bb
 
@@ -150,7 +163,7 @@ def test_gate_score_gradient_through_kept_rows():
     Q64, K64, V64 = (I.bf16_bits_to_f64(at[k]) for k in ("Q", "K", "V"))
     rng = np.random.default_rng(300 + 9)
     dO64 = I.bf16_bits_to_f64(I.f32_to_bf16_bits(rng.standard_normal((M, wl.H_q, wl.d_h)).astype(np.float32)))
-    bb = _d_rounding_bounds(Q64, K64, V64, g.astype(np.float64), dO64, cu, tau, beta)[3]
+    bb = _rounding_bounds(Q64, K64, V64, g.astype(np.float64), dO64, cu, tau, beta)[3]
     tol = np.zeros(T)
     tol[kept] = (bb @ beta.astype(np.float64)) * (1.0 - g) + 1e-4 * float(np.max(np.abs(want))) + 1e-7
     assert np.all(np.abs(got - want) <= tol)

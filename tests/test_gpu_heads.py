@@ -15,7 +15,7 @@ from learned_token_pruning_07_b300 import inputs as I
 from oracle import tokengate_oracle as O
 from tests._helpers import (ATTN_MAX_ABS, ATTN_MEAN_REL, G_ATOL, S_ATOL, S_RTOL, attention_close, bf16_dev_to_f64,
                             dev, host, sampled_rows, status_word, zeros_i32)
-from tests.test_gpu_backward import _d_rounding_bounds
+from tests.test_gpu_backward import _rounding_bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +68,7 @@ def _score_heads(wl, H_g, b1=None, rmsnorm=False, ln_eps=1e-6, rows=None):
         x = h64 / np.sqrt(np.mean(h64 * h64, axis=1, keepdims=True) + ln_eps)
         W1w = I.bf16_bits_to_f64(W1_bits) * I.bf16_bits_to_f64(ln_bits)[None, :]
         var = ((W1w ** 2) @ (x ** 2).T).T @ (W2 ** 2).T                                  # [rows, H_g]
-        tol = tol + 6.0 * 1.1 * 2.0 ** -9 / np.sqrt(3.0) * np.sqrt(var)
+        tol = tol + 6.0 * 1.1 * 2.0 ** -8 / np.sqrt(3.0) * np.sqrt(var)
     got_s = s_h[:T][r]
     assert np.all(np.abs(got_s - ref_s) <= tol)
     np.testing.assert_allclose(g_h[:T][r], ref_g, rtol=0, atol=G_ATOL)
@@ -293,7 +293,7 @@ def test_backward_with_per_head_gates_and_score_gradient():
     tau, beta = at["tau"].astype(np.float64), at["beta"].astype(np.float64)
     np.testing.assert_allclose(host(lse), O.gated_attention_lse(Q64, K64, G64, cu, tau, beta), rtol=0, atol=1e-3)
     ref = O.gated_attention_bwd(Q64, K64, V64, G64, dO64, cu, tau, beta)
-    bounds = _d_rounding_bounds_heads(Q64, K64, V64, G64, dO64, cu, tau, beta)
+    bounds = _rounding_bounds(Q64, K64, V64, G64, dO64, cu, tau, beta)
     for name, a, b, bnd in zip(("dQ", "dK", "dV", "dbias"), [host(t).astype(np.float64) for t in out], ref, bounds):
         tol = bnd + 1e-4 * float(np.max(np.abs(b))) + 1e-7
         assert np.all(np.abs(a - b) <= tol), (name, float(np.abs(a - b).max()))
@@ -304,19 +304,3 @@ def test_backward_with_per_head_gates_and_score_gradient():
         hs = slice(c * per, (c + 1) * per)
         tol_ds[kept, c] = (bounds[3][:, hs] @ beta[hs]) * (1.0 - G64[:, c]) + 1e-4 * float(np.max(np.abs(want))) + 1e-7
     assert np.all(np.abs(host(ds) - want) <= tol_ds)
-
-
-def _d_rounding_bounds_heads(Q, K, V, G, dO, cu, tau, beta):
-    """The backward's first-order bound for the bf16 rounding of O inside D_i (the derivation of
-    the single-gate backward test), with query head h reading gate column h / (H_q / H_g)."""
-    H_q, H_g = Q.shape[1], G.shape[1]
-    per = H_q // H_g
-    parts = [_d_rounding_bounds(Q[:, h:h + 1], K[:, (h * K.shape[1]) // H_q][:, None],
-                                V[:, (h * K.shape[1]) // H_q][:, None], G[:, h // per], dO[:, h:h + 1], cu,
-                                tau[h:h + 1], beta[h:h + 1]) for h in range(H_q)]
-    bq = np.concatenate([p[0] for p in parts], axis=1)
-    bb = np.concatenate([p[3] for p in parts], axis=1)
-    bk = np.zeros_like(K)
-    for h in range(H_q):
-        bk[:, (h * K.shape[1]) // H_q] += parts[h][1][:, 0]
-    return bq, bk, np.zeros_like(V), bb

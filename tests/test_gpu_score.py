@@ -98,16 +98,17 @@ def _rmsnorm_case(wl, rows=None, ln_eps=1e-6):
     ref_s, ref_g = O.gate_score(I.bf16_bits_to_f64(h_bits[sel]), I.bf16_bits_to_f64(gi["W1"]),
                                 I.bf16_bits_to_f64(gi["w2"]), gi["instr_mask"][sel],
                                 ln_weight=I.bf16_bits_to_f64(ln_bits), ln_eps=ln_eps)
-    # The folded weight adds one bf16 rounding (round to nearest: relative error uniform in
-    # +-2^-9, independent per entry) to every W1 diag(w_ln) entry. To first order it moves s by
+    # The folded weight adds one bf16 rounding to every W1 diag(w_ln) entry: round to nearest with
+    # an 8-bit significand, so a relative error e_kc of at most 2^-8 (the unit roundoff), taken as
+    # uniform and independent per entry. To first order it moves s by
     # sum_k w2_k SiLU'(u_k) sum_c e_kc W1w_kc x_c, x = h / rms; with |SiLU'| <= 1.1 its standard
-    # deviation is at most sigma = 1.1 * 2^-9 / sqrt(3) * sqrt(sum_k w2_k^2 sum_c (W1w_kc x_c)^2).
+    # deviation is at most sigma = 1.1 * 2^-8 / sqrt(3) * sqrt(sum_k w2_k^2 sum_c (W1w_kc x_c)^2).
     # Allowed: 6 sigma on top of the plain score tolerance (fp32 accumulation).
     h64 = I.bf16_bits_to_f64(h_bits[sel])
     x = h64 / np.sqrt(np.mean(h64 * h64, axis=1, keepdims=True) + ln_eps)
     W1w = I.bf16_bits_to_f64(gi["W1"]) * I.bf16_bits_to_f64(ln_bits)[None, :]
     var = (I.bf16_bits_to_f64(gi["w2"]) ** 2) @ ((W1w ** 2) @ (x ** 2).T)        # [rows]
-    sigma = 1.1 * 2.0 ** -9 / np.sqrt(3.0) * np.sqrt(var)
+    sigma = 1.1 * 2.0 ** -8 / np.sqrt(3.0) * np.sqrt(var)
     err = np.abs(s_h[:T][sel] - ref_s)
     assert np.all(err <= 6.0 * sigma + S_ATOL + S_RTOL * np.abs(ref_s)), float(np.max(err / (6.0 * sigma + S_ATOL)))
     assert float(np.mean(err)) < 2.0 * float(np.mean(sigma)) + S_ATOL          # and typical errors are ~sigma
