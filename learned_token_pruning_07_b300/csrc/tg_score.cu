@@ -14,7 +14,8 @@
 // other buffer. A row's partial w2 dots of its slices are summed in registers by the same
 // thread, in slice order, so s is deterministic and no scratch memory is needed.
 //
-// Warp roles: warp 0 lane 0 issues TMA; warp 1 owns tensor memory and lane 0 issues MMAs;
+// Warp roles: warp 0 lane 0 issues TMA; warp 1 owns tensor memory and issues MMAs (the warp runs
+// converged and one elected lane issues);
 // warps 2-5 run the epilogue (warp w reads tensor-memory lanes 32*(w%4) .. +31, one row per
 // thread). Every wait is bounded (see tg_set_wait_limit_ns); a wait that gives up sets
 // TG_DEV_TIMEOUT, drains the copies and MMAs in flight, frees tensor memory and returns.
@@ -81,12 +82,13 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
       : "memory");
 }
 
-// Arrive once on the barrier at this offset in both CTAs of the pair when every MMA issued
-// so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
+// Arrive once on the barrier at this offset in both CTAs of the pair when every MMA issued so
+// far by the warp's elected lane has completed.
+__device__ __forceinline__ void mma_commit_pair_elect(uint64_t *bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(tg::smem_u32(bar)),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(tg::smem_u32(bar)),
       "h"(static_cast<uint16_t>((1u << kPair) - 1u))
       : "memory");
 }
@@ -207,15 +209,17 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer: u_slice[128 x item_n] += A[128 x 16] * B[item_n x 16]^T ----
+    {
+      // ---- MMA issuer (converged warp, elected lane): u_slice[128 x item_n] += A[128 x 16] * B[item_n x 16]^T ----
       const uint32_t idesc = tg::idesc_bf16_f32(kBM, p.item_n);
+      const uint64_t a0 = tg::smem_desc(tg::smem_u32(sA), 16, 1024, tg::kSwz128);
+      const uint64_t b0 = tg::smem_desc(tg::smem_u32(sB), 16, 1024, tg::kSwz128);
       int kc = 0, it = 0;
       bool ok = true;
       for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
         for (int item = 0; item < p.n_items && ok; ++item, ++it) {
           const int buf = it & 1;
-          if (!tg::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1u, vabort, p.wait_limit)) {
+          if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1u, vabort, p.wait_limit))) {
             ok = false;
             break;
           }
@@ -223,29 +227,25 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
           const uint32_t d_tmem = tmem + buf * kMaxItemN;
           for (int kt = 0; kt < p.KT; ++kt, ++kc) {
             const int st = kc % kStages;
-            if (!tg::mbar_wait(&full[st], (kc / kStages) & 1, vabort, p.wait_limit)) {
+            if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&full[st], (kc / kStages) & 1, vabort, p.wait_limit))) {
               ok = false;
               break;
             }
             tg::tc_fence_after();
-            const uint32_t a_base = tg::smem_u32(sA + st * L.a_bytes);
-            const uint32_t b_base = tg::smem_u32(sB + st * L.b_bytes);
+            const uint64_t ad = a0 + ((st * L.a_bytes) >> 4), bd = b0 + ((st * L.b_bytes) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kBK / 16; ++ks) {
-              const uint64_t a_desc = tg::smem_desc(a_base + ks * 32, 16, 1024, tg::kSwz128);
-              const uint64_t b_desc = tg::smem_desc(b_base + ks * 32, 16, 1024, tg::kSwz128);
-              tg::mma_bf16_ss(d_tmem, a_desc, b_desc, idesc, (kt | ks) != 0);
-            }
-            mma_commit_pair(&empty[st]);  // the stage is free once both CTAs have read it
-            *n_consumed = kc + 1;
+            for (int ks = 0; ks < kBK / 16; ++ks)  // a K-step of 16 is 32 bytes into the 128-byte row
+              tg::mma_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
+            mma_commit_pair_elect(&empty[st]);  // the stage is free once both CTAs have read it
+            if (lane == 0) *n_consumed = kc + 1;
           }
-          if (ok) tg::mma_commit(&acc_full[buf]);
+          if (ok) tg::mma_commit_elect(&acc_full[buf]);
         }
       }
       if (!ok) {
         *vabort = 1;
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
-        tg::mma_commit(drain);
+        tg::mma_commit_elect(drain);
         volatile int32_t never = 0;
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
