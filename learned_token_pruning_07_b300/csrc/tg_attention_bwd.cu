@@ -82,6 +82,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (Blackwell .f32x2 arithmetic).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Sequence bounds of sequence b clamped to the capacity; false (and TG_DEV_BAD_SEQLENS) when
 // cu_kept is not a valid partition there.
 __device__ __forceinline__ bool seq_bounds(const BwdParams &p, int b, int &start, int &len) {
@@ -332,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dd = p.dQ[row * D];
         }
         dst[q] = negl;
-        dst[128 + q] = dd;
+        dst[128 + q] = -dd;  // -D_i: the elementwise step adds it
       }
       tg::mbar_arrive(&col_full[slot]);
     }
@@ -362,8 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = barrier_all(1, 256, w);  // the same decision in all eight warps
       if (!ok) break;
       tg::tc_fence_after();
-      const float *negl = sCols + slot * 256, *dd = negl + 128;
+      const float *negl = sCols + slot * 256, *negd = negl + 128;
       const bool diag = qt == kt;
+      const uint64_t c2x = f2(c2, c2), chx = f2(ch, ch), b2x = f2(bias2, bias2);
+      uint64_t db2[2] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int c0 = 64 * hh + 32 * chunk;
@@ -371,26 +398,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + c0, sv);
         tg::tmem_ld_32x32b_x32(lane_addr + C::kColDP + c0, dpv);
         tg::tmem_ld_wait();
+        const float4 *nl4 = reinterpret_cast<const float4 *>(negl + c0);
+        const float4 *nd4 = reinterpret_cast<const float4 *>(negd + c0);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pr[2], xr[2];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 nl = nl4[c4], nd = nd4[c4];
+          const float nlv[4] = {nl.x, nl.y, nl.z, nl.w}, ndv[4] = {nd.x, nd.y, nd.z, nd.w};
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c0 + c + e;
-            float pv = ex2(fmaf(__uint_as_float(sv[c + e]), c2, bias2 + negl[col]));
-            if (diag && col < k) pv = 0.0f;  // query before key: not visible
-            const float x = pv * (__uint_as_float(dpv[c + e]) - dd[col]);
-            dbias_acc += x;
-            pr[e] = pv;
-            xr[e] = x * ch;
+          for (int u = 0; u < 2; ++u) {
+            const int c = 4 * c4 + 2 * u;  // columns c0 + c, c0 + c + 1
+            const uint64_t xl = f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2x,
+                                       f2_add(b2x, f2(nlv[2 * u], nlv[2 * u + 1])));
+            float x0, x1;
+            f2_split(xl, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (diag) {  // query before key: not visible
+              if (c0 + c < k) p0 = 0.0f;
+              if (c0 + c + 1 < k) p1 = 0.0f;
+            }
+            const uint64_t pp = f2(p0, p1);
+            const uint64_t xx = f2_mul(pp, f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                                  f2(ndv[2 * u], ndv[2 * u + 1])));
+            db2[u] = f2_add(db2[u], xx);
+            float s0, s1;
+            f2_split(f2_mul(xx, chx), s0, s1);
+            pk[c / 2] = tg::pack_bf16x2(p0, p1);
+            xk[c / 2] = tg::pack_bf16x2(s0, s1);
           }
-          pk[c / 2] = tg::pack_bf16x2(pr[0], pr[1]);
-          xk[c / 2] = tg::pack_bf16x2(xr[0], xr[1]);
         }
         // packed P^T / c dX^T of these 32 queries: 16 columns at the start of this half's S^T / dP^T
         // columns (already read: chunk 0 wrote over its own, chunk 1 over chunk 0's)
         tg::tmem_st_32x32b_x16(lane_addr + C::kColS + 64 * hh + 16 * chunk, pk);
         tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_split(db2[0], a0, a1);
+        f2_split(db2[1], b0, b1);
+        dbias_acc += (a0 + a1) + (b0 + b1);
       }
       tg::tmem_st_wait();
       tg::tc_fence_before();
@@ -647,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::tc_fence_after();
       const float *bias = sCols + slot * 256;
       const bool diag = j == qt;
+      const uint64_t c2x = f2(c2, c2), chx = f2(ch, ch), nlx = f2(negl, negl), ndx = f2(-dd, -dd);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int c0 = 64 * hh + 32 * chunk;
@@ -654,17 +700,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + c0, sv);
         tg::tmem_ld_32x32b_x32(lane_addr + C::kColDP + c0, dpv);
         tg::tmem_ld_wait();
+        const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float xr[2];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 bv = b4[c4];
+          const float bvv[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c0 + c + e;
-            float pv = ex2(fmaf(__uint_as_float(sv[c + e]), c2, bias[col] + negl));
-            if (diag && col > r) pv = 0.0f;  // key after query: not visible
-            xr[e] = pv * (__uint_as_float(dpv[c + e]) - dd) * ch;
+          for (int u = 0; u < 2; ++u) {
+            const int c = 4 * c4 + 2 * u;
+            const uint64_t xl = f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2x,
+                                       f2_add(nlx, f2(bvv[2 * u], bvv[2 * u + 1])));
+            float x0, x1;
+            f2_split(xl, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (diag) {  // key after query: not visible
+              if (c0 + c > r) p0 = 0.0f;
+              if (c0 + c + 1 > r) p1 = 0.0f;
+            }
+            float s0, s1;
+            f2_split(f2_mul(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), ndx)),
+                            chx), s0, s1);
+            xk[c / 2] = tg::pack_bf16x2(s0, s1);
           }
-          xk[c / 2] = tg::pack_bf16x2(xr[0], xr[1]);
         }
         tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
       }
