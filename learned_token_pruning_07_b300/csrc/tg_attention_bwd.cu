@@ -400,25 +400,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::tmem_ld_wait();
         const float4 *nl4 = reinterpret_cast<const float4 *>(negl + c0);
         const float4 *nd4 = reinterpret_cast<const float4 *>(negd + c0);
+        // phase 1: the 32 logits in log2 units, in place
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 nl = nl4[c4], nd = nd4[c4];
-          const float nlv[4] = {nl.x, nl.y, nl.z, nl.w}, ndv[4] = {nd.x, nd.y, nd.z, nd.w};
+          const float4 nl = nl4[c4];
+          const uint64_t a = f2_fma(f2(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), c2x,
+                                    f2_add(b2x, f2(nl.x, nl.y)));
+          const uint64_t b = f2_fma(f2(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), c2x,
+                                    f2_add(b2x, f2(nl.z, nl.w)));
+          float a0, a1, b0, b1;
+          f2_split(a, a0, a1);
+          f2_split(b, b0, b1);
+          sv[4 * c4] = __float_as_uint(a0);
+          sv[4 * c4 + 1] = __float_as_uint(a1);
+          sv[4 * c4 + 2] = __float_as_uint(b0);
+          sv[4 * c4 + 3] = __float_as_uint(b1);
+        }
+        // phase 2: the 32 exponentials back to back
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(ex2(__uint_as_float(sv[c])));
+        if (diag) {  // query before key: not visible
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c0 + c < k) sv[c] = 0u;
+        }
+        // phase 3: dX = P (dP - D), the bias gradient, and the bf16 operands
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 nd = nd4[c4];
+          const float ndv[4] = {nd.x, nd.y, nd.z, nd.w};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int c = 4 * c4 + 2 * u;  // columns c0 + c, c0 + c + 1
-            const uint64_t xl = f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2x,
-                                       f2_add(b2x, f2(nlv[2 * u], nlv[2 * u + 1])));
-            float x0, x1;
-            f2_split(xl, x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (diag) {  // query before key: not visible
-              if (c0 + c < k) p0 = 0.0f;
-              if (c0 + c + 1 < k) p1 = 0.0f;
-            }
-            const uint64_t pp = f2(p0, p1);
-            const uint64_t xx = f2_mul(pp, f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
-                                                  f2(ndv[2 * u], ndv[2 * u + 1])));
+            const int c = 4 * c4 + 2 * u;
+            const float p0 = __uint_as_float(sv[c]), p1 = __uint_as_float(sv[c + 1]);
+            const uint64_t xx = f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                                          f2(ndv[2 * u], ndv[2 * u + 1])));
             db2[u] = f2_add(db2[u], xx);
             float s0, s1;
             f2_split(f2_mul(xx, chx), s0, s1);
@@ -426,8 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             xk[c / 2] = tg::pack_bf16x2(s0, s1);
           }
         }
-        // packed P^T / c dX^T of these 32 queries: 16 columns at the start of this half's S^T / dP^T
-        // columns (already read: chunk 0 wrote over its own, chunk 1 over chunk 0's)
         tg::tmem_st_32x32b_x16(lane_addr + C::kColS + 64 * hh + 16 * chunk, pk);
         tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
       }
@@ -704,24 +718,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 bv = b4[c4];
-          const float bvv[4] = {bv.x, bv.y, bv.z, bv.w};
+          const uint64_t a = f2_fma(f2(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), c2x,
+                                    f2_add(nlx, f2(bv.x, bv.y)));
+          const uint64_t b = f2_fma(f2(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), c2x,
+                                    f2_add(nlx, f2(bv.z, bv.w)));
+          float a0, a1, b0, b1;
+          f2_split(a, a0, a1);
+          f2_split(b, b0, b1);
+          sv[4 * c4] = __float_as_uint(a0);
+          sv[4 * c4 + 1] = __float_as_uint(a1);
+          sv[4 * c4 + 2] = __float_as_uint(b0);
+          sv[4 * c4 + 3] = __float_as_uint(b1);
+        }
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 4 * c4 + 2 * u;
-            const uint64_t xl = f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2x,
-                                       f2_add(nlx, f2(bvv[2 * u], bvv[2 * u + 1])));
-            float x0, x1;
-            f2_split(xl, x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (diag) {  // key after query: not visible
-              if (c0 + c > r) p0 = 0.0f;
-              if (c0 + c + 1 > r) p1 = 0.0f;
-            }
-            float s0, s1;
-            f2_split(f2_mul(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), ndx)),
-                            chx), s0, s1);
-            xk[c / 2] = tg::pack_bf16x2(s0, s1);
-          }
+        for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(ex2(__uint_as_float(sv[c])));
+        if (diag) {  // key after query: not visible
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c0 + c > r) sv[c] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float s0, s1;
+          f2_split(f2_mul(f2_mul(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                 f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), ndx)),
+                          chx), s0, s1);
+          xk[c / 2] = tg::pack_bf16x2(s0, s1);
         }
         tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
       }
