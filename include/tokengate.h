@@ -371,11 +371,12 @@ TG_API tg_status tg_set_wait_limit_ns(uint64_t limit_ns);
  *   counterpart in the TokenGate pages). While a bit is set, the matching kernel's copy
  *   producer issues none of its loads, so the consumers' waits run out after the wait limit;
  *   the kernel sets TG_DEV_TIMEOUT, frees its tensor memory and returns, and the CUDA context
- *   stays usable. Nothing faults or hangs. Bits: TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION;
+ *   stays usable. Nothing faults or hangs. Bits: TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION,
+ *   TG_WITHHOLD_BACKWARD (the dK/dV and dQ passes of tg_gated_attention_bwd);
  *   0 (the default) clears them. Any other bit is TG_ERR_INVALID_ARG. Process-wide; takes
  *   effect for later launches.
  */
-enum { TG_WITHHOLD_GATE_SCORE = 1 << 0, TG_WITHHOLD_ATTENTION = 1 << 1 };
+enum { TG_WITHHOLD_GATE_SCORE = 1 << 0, TG_WITHHOLD_ATTENTION = 1 << 1, TG_WITHHOLD_BACKWARD = 1 << 2 };
 TG_API tg_status tg_set_test_withhold(int32_t mask);
 
 #ifdef __cplusplus

@@ -52,6 +52,7 @@ struct BwdParams {
   float *dQ, *dK, *dV, *dbias;
   int32_t *status;
   uint64_t wait_limit, drain_limit;
+  int32_t withhold;  // test hook: the TMA warps issue no loads, so the consumers' waits run out
   float scale[kMaxHeads];  // c_h = tau_h / sqrt(d_h)
   float beta[kMaxHeads];
 };
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.withhold) {
       // ---------------- TMA: K, V of the key tile once; then (Q, dO) of every iteration ----------------
       tg::mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
       for (int hf = 0; hf < C::kHalves; ++hf) {
@@ -588,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.withhold) {
       // ---------------- TMA: Q, dO of the query tile once; then (K, V) of every key tile ----------------
       tg::mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
       for (int hf = 0; hf < C::kHalves; ++hf) {
@@ -900,6 +901,7 @@ tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const
   p.status = status;
   p.wait_limit = wait_limit_ns();
   p.drain_limit = drain_limit_ns();
+  p.withhold = (withhold_mask() & TG_WITHHOLD_BACKWARD) != 0;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale[h] = h < H_q ? tau[h] / std::sqrt(static_cast<float>(d_h)) : 0.0f;
     p.beta[h] = h < H_q ? beta[h] : 0.0f;

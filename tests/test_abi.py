@@ -96,8 +96,9 @@ def test_wait_limit_setter(lib):
 
 
 def test_test_withhold_hook_validates_its_mask(lib):
-    assert lib.tg_set_test_withhold(binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION) == binding.TG_OK
-    assert lib.tg_set_test_withhold(4) == binding.TG_ERR_INVALID_ARG
+    all_bits = binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION | binding.TG_WITHHOLD_BACKWARD
+    assert lib.tg_set_test_withhold(all_bits) == binding.TG_OK
+    assert lib.tg_set_test_withhold(8) == binding.TG_ERR_INVALID_ARG
     assert lib.tg_set_test_withhold(0) == binding.TG_OK
 
 

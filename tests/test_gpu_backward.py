@@ -109,6 +109,20 @@ def test_backward_varlen_dh128(lens):
     _case(I.WORKLOADS["qwen3_1p7b_8k"], lens, seed=len(lens))
 
 
+def test_backward_at_the_bench_size():
+    # the bench's backward runs on the 32K workload's kept rows at K = 4096: one sequence of
+    # 4,096 document + 256 instruction rows (34 key tiles, both heads of every GQA group)
+    wl = I.WORKLOADS["sweep_32k"]
+    _case(wl, [wl.K + wl.instr_lens[0]], seed=41)
+
+
+def test_backward_ragged_batch_kept_lengths():
+    # the first three sequences of the ragged batch as the prune step keeps them at K = 2048
+    wl = I.WORKLOADS["ragged_b8"]
+    lens = [min(wl.K, d) + n for d, n in zip(wl.doc_lens[:3], wl.instr_lens[:3])]
+    _case(I.WORKLOADS["qwen3_1p7b_8k"], lens, seed=42)
+
+
 def test_backward_mha_and_odd_group():
     _case(I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=4, H_kv=4), [130, 70], seed=21)
     _case(I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=6, H_kv=2), [130, 70], seed=22)

@@ -92,3 +92,30 @@ def test_timeout_is_translated_by_read_device_status(withheld):
     code = tg.load().tg_read_device_status(st.data_ptr(), out.ctypes.data,
                                           torch.cuda.current_stream().cuda_stream)
     assert code == tg.TG_ERR_DEVICE_TIMEOUT and out[0] & tg.TG_DEV_TIMEOUT
+
+
+def test_backward_wait_runs_out_then_recovers(withheld):
+    # the dK/dV and dQ passes: their TMA warps issue nothing, so the MMA warp, the column
+    # producer and the eight elementwise warps (which agree through barrier.red before leaving)
+    # all give up after the limit; the next call, with the hook cleared, matches the oracle
+    from tests.test_gpu_backward import _case
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    lens = [300, 129]
+    cu = I.cu_seqlens_of(lens)
+    M = int(cu[-1])
+    at = I.make_attention_inputs(wl, M)
+    Qd, Kd, Vd, gd, cud = dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(at["g"]), dev(cu)
+    O_d = torch.zeros((M, wl.H_q, wl.d_h), dtype=torch.int16, device="cuda")
+    lse = torch.zeros((M, wl.H_q), dtype=torch.float32, device="cuda")
+    st = status_word()
+    withheld(tg.TG_WITHHOLD_BACKWARD)
+    tg.gated_attention_lse(Qd, Kd, Vd, cud, at["tau"], at["beta"], O_d, lse, max_seqlen=max(lens), g=gd, status=st)
+    assert tg.read_device_status(st) == 0  # the forward is not withheld
+    f = lambda *shape: torch.zeros(shape, dtype=torch.float32, device="cuda")
+    tg.gated_attention_bwd(Qd, Kd, Vd, O_d, O_d, lse, cud, at["tau"], at["beta"], f(M, wl.H_q, wl.d_h),
+                           f(M, wl.H_kv, wl.d_h), f(M, wl.H_kv, wl.d_h), f(M, wl.H_q), max_seqlen=max(lens), g=gd,
+                           status=st)
+    assert tg.read_device_status(st) & tg.TG_DEV_TIMEOUT
+    tg.set_test_withhold(0)
+    tg.set_wait_limit_ns(0)
+    _case(wl, lens, seed=5)
