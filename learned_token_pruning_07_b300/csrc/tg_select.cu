@@ -13,7 +13,10 @@
 // bins from the eight CTAs (two small remote rounds instead of pulling whole histograms,
 // since DSMEM bandwidth, not latency, dominated), and every CTA picks the same digit. After the
 // third pass the threshold key T and the number of ties at T to keep are exact; ties are
-// granted to the lowest indices. Compaction: each warp owns a contiguous segment of its
+// granted to the lowest indices. When, after the first or second pass, the chosen bin holds
+// exactly as many keys as are still needed (the usual case for continuous scores after 22
+// bits), the whole bin is kept: T is set just below the bin with no ties to split, and the
+// remaining passes are skipped. The kept set is the same either way. Compaction: each warp owns a contiguous segment of its
 // CTA's chunk; per-warp counts of keys above / at T and of instruction rows, one DSMEM
 // exchange of CTA totals, and one ballot-prefix pass per warp write the kept indices in
 // order. No global scratch memory and no waits between clusters: the output offset of
@@ -122,7 +125,8 @@ struct SelShared {
   int32_t coarse[2][kCoarse]; // sums of 32 consecutive fine bins, same buffering
   int32_t ctot[kCoarse];      // cluster-wide coarse totals
   int32_t ftot[kFine];        // cluster-wide counts of the fine bins inside the chosen coarse bin
-  int32_t pick[4][4];         // per pass: coarse bin, keys needed in it, digit, keys needed in it
+  int32_t pick[3][5];         // per pass: coarse bin, keys needed in it, digit, keys needed in it,
+                              // keys in that digit's bin
   int32_t n_need;             // keys the selection takes: min(K, document rows)
   int32_t wgt[kWarps], weq[kWarps], wnm[kWarps];
   int32_t woff[kWarps], wtie[kWarps];
@@ -238,6 +242,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   int need = 0;
   int seq_offset = 0;
   bool select_none = false;
+  bool early = false;
+  uint32_t early_t = 0u;
   for (int pass = 0; pass < 3; ++pass) {
     int32_t *hist = sh.hist[pass & 1];
     reinterpret_cast<int4 *>(hist)[tid] = make_int4(0, 0, 0, 0);
@@ -245,7 +251,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int width = pass < 2 ? 11 : 10;
     const uint32_t dmask = (1u << width) - 1u;
-    for (int i = tid; i < len; i += kThreads) {
+    // four keys in flight per thread: the shared-memory loads go out before the atomics
+    int i = tid;
+    for (; i + 3 * kThreads < len; i += 4 * kThreads) {
+      uint32_t k4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) k4[u] = key_at(i + u * kThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (k4[u] != 0u && (pass == 0 || (k4[u] >> (shift + width)) == prefix))
+          atomicAdd(&hist[(k4[u] >> shift) & dmask], 1);
+    }
+    for (; i < len; i += kThreads) {
       const uint32_t key = key_at(i);
       if (key != 0u && (pass == 0 || (key >> (shift + width)) == prefix))
         atomicAdd(&hist[(key >> shift) & dmask], 1);
@@ -312,14 +329,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       if (above < nd && nd <= above + cnt) {
         sh.pick[pass][2] = cbin * kFine + lane;
         sh.pick[pass][3] = nd - above;
+        sh.pick[pass][4] = cnt;
       }
     }
     __syncthreads();
     prefix = (prefix << width) | static_cast<uint32_t>(sh.pick[pass][2]);
     need = sh.pick[pass][3];
+    if (pass < 2 && need == sh.pick[pass][4] && prefix != 0u) {
+      // every key of the chosen bin is kept: the threshold sits just below the bin, with no
+      // ties to split, and the remaining passes are not needed (uniform: every CTA of the
+      // cluster read the same counts)
+      early_t = (prefix << shift) - 1u;
+      early = true;
+      break;
+    }
   }
-  const uint32_t T = select_none ? 0xFFFFFFFFu : prefix;
-  const int need_ties = select_none ? 0 : need;
+  const uint32_t T = select_none ? 0xFFFFFFFFu : (early ? early_t : prefix);
+  const int need_ties = (select_none || early) ? 0 : need;
 
   // ---- per-warp counts over contiguous warp segments ----
   const int seg = 32 * ((chunk + kThreads - 1) / kThreads);

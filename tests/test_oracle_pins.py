@@ -38,9 +38,9 @@ def test_gate_score_closed_form():
     np.testing.assert_allclose(g, fx["g"], rtol=0, atol=1e-14)
 
 
-@pytest.mark.parametrize("with_bias", [False, True])
-def test_gate_score_matches_torch_mlp(with_bias):
-    wl = I.WORKLOADS["tiny"]
+@pytest.mark.parametrize("name,with_bias", [("tiny", False), ("tiny", True), ("qwen3_1p7b_8k", True)])
+def test_gate_score_matches_torch_mlp(name, with_bias):
+    wl = I.WORKLOADS[name]
     gi = I.make_gate_inputs(wl)
     h = I.bf16_bits_to_f64(gi["h"])
     W1 = I.bf16_bits_to_f64(gi["W1"])
