@@ -262,6 +262,9 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       float acc[GHP];
 #pragma unroll
       for (int c = 0; c < GHP; ++c) acc[c] = 0.0f;
+      uint64_t acc2[GHP > 1 ? GHP / 2 : 1];  // head pairs (2k, 2k + 1) as packed fp32
+#pragma unroll
+      for (int k = 0; k < (GHP > 1 ? GHP / 2 : 1); ++k) acc2[k] = 0ull;
       float inv_rms = 1.0f;
       if (NORM) {
         ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&rms_ready[ti & 1], (ti >> 1) & 1, vabort, p.wait_limit));
@@ -301,10 +304,13 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
 #pragma unroll
                 for (int k = 0; k < GHP / 2; ++k) w[k] = src[k];
               }
+              uint64_t silu2;
+              asm("mov.b64 %0, {%1, %1};" : "=l"(silu2) : "f"(silu));
 #pragma unroll
               for (int k = 0; k < GHP / 2; ++k) {
-                acc[2 * k] = fmaf(__uint_as_float(w[k] << 16), silu, acc[2 * k]);
-                acc[2 * k + 1] = fmaf(__uint_as_float(w[k] & 0xFFFF0000u), silu, acc[2 * k + 1]);
+                uint64_t wk;  // the bf16 pair widened to fp32: low half, then high half
+                asm("mov.b64 %0, {%1, %2};" : "=l"(wk) : "r"(w[k] << 16), "r"(w[k] & 0xFFFF0000u));
+                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[k]) : "l"(wk), "l"(silu2));
               }
             }
           }
@@ -314,6 +320,11 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
         if (lane == 0) tg::mbar_arrive(&acc_empty[buf]);
       }
       if (!ok) break;
+      if constexpr (GHP > 1) {
+#pragma unroll
+        for (int k = 0; k < GHP / 2; ++k)
+          asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * k]), "=f"(acc[2 * k + 1]) : "l"(acc2[k]));
+      }
       if (NORM) {
         __syncwarp();
         if (lane == 0) tg::mbar_arrive(&rms_free[ti & 1]);  // this tile's 1/rms slots are free
