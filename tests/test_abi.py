@@ -160,3 +160,38 @@ def test_gate_score_heads_entry_points_reject_bad_arguments(lib):
     s = lib.tg_gate_score_grad
     beta = np.ones(4, np.float32)
     assert s(p, beta.ctypes.data, p, 3, p, p, 1, 8, 4, 16, p, None) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_backward_entry_points_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    tau = np.ones(4, np.float32)
+    beta = np.ones(4, np.float32)
+    # tg_gated_attention_lse: the log-sum-exp output is required
+    lse = lambda out: lib.tg_gated_attention_lse(p, p, p, None, 1, p, 1, 64, 64, 4, 2, 64, tau.ctypes.data,
+                                                 beta.ctypes.data, p, out, None, None)
+    assert lse(None) == binding.TG_ERR_INVALID_ARG
+    # tg_gated_attention_bwd: dO, lse and every gradient buffer are required; shapes as the forward
+    bwd = lambda dO=p, lse_=p, dq=p, dbias=p, dh=64, hg=1: lib.tg_gated_attention_bwd(
+        p, p, p, None, hg, p, dO, lse_, p, 1, 64, 64, 4, 2, dh, tau.ctypes.data, beta.ctypes.data,
+        dq, p, p, dbias, None, None)
+    assert bwd(dO=None) == binding.TG_ERR_INVALID_ARG
+    assert bwd(lse_=None) == binding.TG_ERR_INVALID_ARG
+    assert bwd(dq=None) == binding.TG_ERR_INVALID_ARG
+    assert bwd(dbias=None) == binding.TG_ERR_INVALID_ARG
+    assert bwd(dh=96) == binding.TG_ERR_UNSUPPORTED
+    assert bwd(hg=3) == binding.TG_ERR_UNSUPPORTED
+
+
+def test_prune_layer_entry_points_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    layer = lambda g_out=p, K=8, d=256, d_g=64, b2=0.0: lib.tg_gate_prune_layer(
+        p, None, None, p, 1, 128, d, p, None, p, b2, d_g, K, p, g_out, p, 128, p, p, None, None, None, None)
+    assert layer(g_out=None) == binding.TG_ERR_INVALID_ARG        # the gate buffer is required here
+    assert layer(K=-1) == binding.TG_ERR_INVALID_ARG
+    assert layer(b2=float("inf")) == binding.TG_ERR_INVALID_ARG
+    assert layer(d=100) == binding.TG_ERR_UNSUPPORTED             # d % 32 != 0
+    assert layer(d_g=1024) == binding.TG_ERR_UNSUPPORTED          # d_g > 512
+    two = lambda capacity: lib.tg_two_budget_prune_layer(
+        p, None, None, p, 1, 128, 256, p, None, p, 0.0, 64, 8, p, p, p, capacity, p, p, None, None, None, None)
+    assert two(127) == binding.TG_ERR_INVALID_ARG                 # the full half alone is T_total rows
+    assert lib.tg_read_device_status(None, None, None) == binding.TG_ERR_INVALID_ARG
