@@ -75,6 +75,9 @@ struct BwdCfg {
   static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
   // tensor memory columns: S (or S^T), dP (or dP^T), then the accumulators
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  // pass 3 keeps one accumulator, so dP (and c dX in its place) alternates between kColDP and 384
+  static __device__ __forceinline__ uint32_t dp_col(int j) { return (j & 1) ? 384u : kColDP; }
+  static_assert(D <= 128, "pass 3's second dP block starts at column 384");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -200,9 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *kv_full = bars;
   uint64_t *ring_full = kv_full + 1;               // [kStages]
   uint64_t *ring_empty = ring_full + C::kStages;   // [kStages]
-  uint64_t *st_full = ring_empty + C::kStages;     // S^T and dP^T of the iteration are ready
-  uint64_t *p_full = st_full + 1;                  // P^T and c dX^T written back (8 warps)
-  uint64_t *dv_done = p_full + 1;
+  uint64_t *s_full = ring_empty + C::kStages;      // S^T of the iteration is ready
+  uint64_t *dp_full = s_full + 1;                  // dP^T of the iteration is ready
+  uint64_t *p_full = dp_full + 1;                  // P^T written back (8 warps)
+  uint64_t *x_full = p_full + 1;                   // c dX^T written back (8 warps)
+  uint64_t *dv_done = x_full + 1;
   uint64_t *dk_done = dv_done + 1;
   uint64_t *acc_final = dk_done + 1;
   uint64_t *col_full = acc_final + 1;              // [2]
@@ -238,8 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::mbar_init(&ring_full[s], 1);
       tg::mbar_init(&ring_empty[s], 1);
     }
-    tg::mbar_init(st_full, 1);
+    tg::mbar_init(s_full, 1);
+    tg::mbar_init(dp_full, 1);
     tg::mbar_init(p_full, 8);
+    tg::mbar_init(x_full, 8);
     tg::mbar_init(dv_done, 1);
     tg::mbar_init(dk_done, 1);
     tg::mbar_init(acc_final, 1);
@@ -291,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issue (converged warp, elected lane) ----------------
+    // Software-pipelined: dV(i) starts once P^T(i) is written, S^T(i + 1) refills those columns once
+    // dV(i) has read them, and dK(i) then dP^T(i + 1) follow c dX^T(i) in the same way, so the
+    // products of one iteration run while the elementwise warps work on the other half of it.
     const uint32_t idesc_st = tg::idesc_bf16_f32(kTile, kTile);          // K Q^T, V dO^T: both K-major
     const uint32_t idesc_acc = tg::idesc_bf16_f32(kTile, D, 0, 1);       // P^T dO, dX^T Q: B MN-major
     const uint64_t dk0 = tg::smem_desc(tg::smem_u32(sK), 16, 1024, tg::kSwz128);
@@ -299,34 +309,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dr0_mn = tg::smem_desc(tg::smem_u32(sRing), 16384, 1024, tg::kSwz128);
     constexpr uint32_t kTile16 = C::kTileBytes >> 4;
     bool ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(kv_full, 0, vabort, p.wait_limit));
+    if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&ring_full[0], 0, vabort, p.wait_limit));
     int consumed = 0;
+    if (ok) {  // S^T(0), dP^T(0): ring stage 0 holds Q at tile 0, dO at tile 1
+      consumed = 1;
+      tg::tc_fence_after();
+      mma_tile_ss<D>(tmem + C::kColS, dk0, dr0, idesc_st);
+      tg::mma_commit_elect(s_full);
+      mma_tile_ss<D>(tmem + C::kColDP, dv0, dr0 + kTile16, idesc_st);
+      tg::mma_commit_elect(dp_full);
+    }
     for (int i = 0; i < n_iter && ok; ++i) {
-      const int s = i % C::kStages;
+      const int s = i % C::kStages, s1 = (i + 1) % C::kStages;
       const uint64_t q_off = 2 * s * kTile16, do_off = q_off + kTile16;
-      // S^T overwrites P^T(i - 1), which dV(i - 1) reads; dP^T overwrites dX^T(i - 1), read by dK(i - 1)
-      ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&ring_full[s], (i / C::kStages) & 1, vabort, p.wait_limit));
-      if (ok && i > 0) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(dv_done, (i - 1) & 1, vabort, p.wait_limit));
+      const uint64_t q1_off = 2 * s1 * kTile16, do1_off = q1_off + kTile16;
+      const bool more = i + 1 < n_iter;
+      ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(p_full, i & 1, vabort, p.wait_limit));
       if (!ok) break;
-      consumed = i + 1;
-      tg::tc_fence_after();
-      mma_tile_ss<D>(tmem + C::kColS, dk0, dr0 + q_off, idesc_st);
-      if (i > 0 && !__all_sync(0xFFFFFFFFu, tg::mbar_wait(dk_done, (i - 1) & 1, vabort, p.wait_limit))) {
-        ok = false;
-        break;
-      }
-      tg::tc_fence_after();
-      mma_tile_ss<D>(tmem + C::kColDP, dv0, dr0 + do_off, idesc_st);
-      tg::mma_commit_elect(st_full);
-      if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(p_full, i & 1, vabort, p.wait_limit))) {
-        ok = false;
-        break;
-      }
       tg::tc_fence_after();
       mma_tile_ts<D>(tmem + C::kColAcc0, tmem + C::kColS, dr0_mn + do_off, idesc_acc, i == 0);   // dV
       tg::mma_commit_elect(dv_done);
+      if (more) {  // S^T(i + 1) overwrites P^T(i): after dV(i) has read it
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&ring_full[s1], ((i + 1) / C::kStages) & 1, vabort,
+                                                   p.wait_limit));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(dv_done, i & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        consumed = i + 2;
+        tg::tc_fence_after();
+        mma_tile_ss<D>(tmem + C::kColS, dk0, dr0 + q1_off, idesc_st);
+        tg::mma_commit_elect(s_full);
+      }
+      ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(x_full, i & 1, vabort, p.wait_limit));
+      if (!ok) break;
+      tg::tc_fence_after();
       mma_tile_ts<D>(tmem + C::kColAcc1, tmem + C::kColDP, dr0_mn + q_off, idesc_acc, i == 0);   // dK
       tg::mma_commit_elect(dk_done);
       tg::mma_commit_elect(&ring_empty[s]);
+      if (more) {  // dP^T(i + 1) overwrites c dX^T(i): after dK(i) has read it
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(dk_done, i & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        tg::tc_fence_after();
+        mma_tile_ss<D>(tmem + C::kColDP, dv0, dr0 + do1_off, idesc_st);
+        tg::mma_commit_elect(dp_full);
+      }
     }
     if (ok) tg::mma_commit_elect(acc_final);
     if (lane == 0) flags[2] = consumed;
@@ -364,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------- elementwise: thread = key row, warps 4-7 / 8-11 = query columns 0-63 / 64-127 ----------------
+    // Two halves per iteration: P^T from S^T (signals p_full, so dV starts), then c dX^T from dP^T with
+    // P kept in registers (signals x_full, so dK starts).
     const int wq = warp & 3, hh = (warp - 4) >> 2;
     const int k = wq * 32 + lane, kj = k0 + k;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -383,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ch = p.scale[h];
         c2 = ch * kLog2e;
       }
-      bool w = tg::mbar_wait(st_full, i & 1, vabort, p.wait_limit);
+      bool w = tg::mbar_wait(s_full, i & 1, vabort, p.wait_limit);
       w = w && tg::mbar_wait(&col_full[slot], (i >> 1) & 1, vabort, p.wait_limit);
       ok = barrier_all(1, 256, w);  // the same decision in all eight warps
       if (!ok) break;
@@ -391,17 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *negl = sCols + slot * 256, *negd = negl + 128;
       const bool diag = qt == kt;
       const uint64_t c2x = f2(c2, c2), chx = f2(ch, ch), b2x = f2(bias2, bias2);
-      uint64_t db2[2] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
+      // ---- first half: P^T ----
+      uint32_t pv[2][32];
+      tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + 64 * hh, pv[0]);
+      tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + 64 * hh + 32, pv[1]);
+      tg::tmem_ld_wait();
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int c0 = 64 * hh + 32 * chunk;
-        uint32_t sv[32], dpv[32], pk[16], xk[16];
-        tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + c0, sv);
-        tg::tmem_ld_32x32b_x32(lane_addr + C::kColDP + c0, dpv);
-        tg::tmem_ld_wait();
+        uint32_t *sv = pv[chunk];
         const float4 *nl4 = reinterpret_cast<const float4 *>(negl + c0);
-        const float4 *nd4 = reinterpret_cast<const float4 *>(negd + c0);
-        // phase 1: the 32 logits in log2 units, in place
+        // the 32 logits in log2 units, in place
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 nl = nl4[c4];
@@ -417,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sv[4 * c4 + 2] = __float_as_uint(b0);
           sv[4 * c4 + 3] = __float_as_uint(b1);
         }
-        // phase 2: the 32 exponentials back to back
+        // the 32 exponentials back to back
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(ex2(__uint_as_float(sv[c])));
         if (diag) {  // query before key: not visible
@@ -425,7 +452,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c)
             if (c0 + c < k) sv[c] = 0u;
         }
-        // phase 3: dX = P (dP - D), the bias gradient, and the bf16 operands
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) pk[c / 2] = tg::pack_bf16x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        tg::tmem_st_32x32b_x16(lane_addr + C::kColS + 64 * hh + 16 * chunk, pk);
+      }
+      tg::tmem_st_wait();
+      tg::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tg::mbar_arrive(p_full);
+      // ---- second half: c dX^T = c P (dP - D), and the bias gradient ----
+      w = tg::mbar_wait(dp_full, i & 1, vabort, p.wait_limit);
+      ok = barrier_all(1, 256, w);
+      if (!ok) break;
+      tg::tc_fence_after();
+      uint64_t db2[2] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
+#pragma unroll
+      for (int chunk = 0; chunk < 2; ++chunk) {
+        const int c0 = 64 * hh + 32 * chunk;
+        const uint32_t *sv = pv[chunk];
+        uint32_t dpv[32], xk[16];
+        tg::tmem_ld_32x32b_x32(lane_addr + C::kColDP + c0, dpv);
+        tg::tmem_ld_wait();
+        const float4 *nd4 = reinterpret_cast<const float4 *>(negd + c0);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 nd = nd4[c4];
@@ -433,17 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int c = 4 * c4 + 2 * u;
-            const float p0 = __uint_as_float(sv[c]), p1 = __uint_as_float(sv[c + 1]);
-            const uint64_t xx = f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
-                                                          f2(ndv[2 * u], ndv[2 * u + 1])));
+            const uint64_t xx = f2_mul(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                       f2_add(f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                              f2(ndv[2 * u], ndv[2 * u + 1])));
             db2[u] = f2_add(db2[u], xx);
             float s0, s1;
             f2_split(f2_mul(xx, chx), s0, s1);
-            pk[c / 2] = tg::pack_bf16x2(p0, p1);
             xk[c / 2] = tg::pack_bf16x2(s0, s1);
           }
         }
-        tg::tmem_st_32x32b_x16(lane_addr + C::kColS + 64 * hh + 16 * chunk, pk);
         tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
       }
       {
@@ -456,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        tg::mbar_arrive(p_full);
+        tg::mbar_arrive(x_full);
         tg::mbar_arrive(&col_empty[slot]);
       }
       if (i % n_q == n_q - 1) {
@@ -527,9 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *qd_full = bars;
   uint64_t *ring_full = qd_full + 1;               // [kStages]
   uint64_t *ring_empty = ring_full + C::kStages;   // [kStages]
-  uint64_t *st_full = ring_empty + C::kStages;
-  uint64_t *p_full = st_full + 1;
-  uint64_t *dq_done = p_full + 1;
+  uint64_t *st_full = ring_empty + C::kStages;     // S and dP of the iteration are ready
+  uint64_t *s_free = st_full + 1;                  // S read into registers (8 warps)
+  uint64_t *p_full = s_free + 1;                   // [2] c dX of iteration j written back (8 warps)
+  uint64_t *dq_done = p_full + 2;
   uint64_t *acc_final = dq_done + 1;
   uint64_t *col_full = acc_final + 1;              // [2]
   uint64_t *col_empty = col_full + 2;              // [2]
@@ -564,7 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::mbar_init(&ring_empty[s], 1);
     }
     tg::mbar_init(st_full, 1);
-    tg::mbar_init(p_full, 8);
+    tg::mbar_init(s_free, 8);
+    tg::mbar_init(&p_full[0], 8);
+    tg::mbar_init(&p_full[1], 8);
     tg::mbar_init(dq_done, 1);
     tg::mbar_init(acc_final, 1);
     for (int s = 0; s < 2; ++s) {
@@ -615,6 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issue (converged warp, elected lane) ----------------
+    // Software-pipelined: S(j + 1) and dP(j + 1) are issued once the elementwise warps hold S(j) in
+    // registers (dP alternates between two column blocks), so they run while c dX(j) is computed;
+    // dQ(j) follows c dX(j).
     const uint32_t idesc_st = tg::idesc_bf16_f32(kTile, kTile);     // Q K^T, dO V^T: both K-major
     const uint32_t idesc_acc = tg::idesc_bf16_f32(kTile, D, 0, 1);  // dX K: B MN-major
     const uint64_t dq0 = tg::smem_desc(tg::smem_u32(sQ), 16, 1024, tg::kSwz128);
@@ -624,30 +677,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kTile16 = C::kTileBytes >> 4;
     bool ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(qd_full, 0, vabort, p.wait_limit));
     int consumed = 0;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j % C::kStages;
-      const uint64_t k_off = 2 * s * kTile16, v_off = k_off + kTile16;
-      // dP overwrites c dX(j - 1), which dQ(j - 1) reads; S(j - 1) was read before p_full(j - 1)
-      ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&ring_full[s], (j / C::kStages) & 1, vabort, p.wait_limit));
-      if (!ok) break;
-      consumed = j + 1;
-      tg::tc_fence_after();
-      mma_tile_ss<D>(tmem + C::kColS, dq0, dr0 + k_off, idesc_st);
-      if (j > 0 && !__all_sync(0xFFFFFFFFu, tg::mbar_wait(dq_done, (j - 1) & 1, vabort, p.wait_limit))) {
-        ok = false;
-        break;
+    for (int j = 0; j <= n_kv && ok; ++j) {
+      if (j < n_kv) {
+        const int s = j % C::kStages;
+        const uint64_t k_off = 2 * s * kTile16, v_off = k_off + kTile16;
+        // S(j) overwrites S(j - 1): after the elementwise warps have read it
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&ring_full[s], (j / C::kStages) & 1, vabort, p.wait_limit));
+        if (ok && j > 0) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(s_free, (j - 1) & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        consumed = j + 1;
+        tg::tc_fence_after();
+        mma_tile_ss<D>(tmem + C::kColS, dq0, dr0 + k_off, idesc_st);
+        if (j >= 2) {  // dP(j) overwrites c dX(j - 2): after dQ(j - 2) has read it
+          ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(dq_done, (j - 2) & 1, vabort, p.wait_limit));
+          if (!ok) break;
+          tg::tc_fence_after();
+        }
+        mma_tile_ss<D>(tmem + C::dp_col(j), ddo0, dr0 + v_off, idesc_st);
+        tg::mma_commit_elect(st_full);
       }
-      tg::tc_fence_after();
-      mma_tile_ss<D>(tmem + C::kColDP, ddo0, dr0 + v_off, idesc_st);
-      tg::mma_commit_elect(st_full);
-      if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(p_full, j & 1, vabort, p.wait_limit))) {
-        ok = false;
-        break;
+      if (j > 0) {
+        const int jp = j - 1, sp = jp % C::kStages;
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&p_full[jp & 1], (jp >> 1) & 1, vabort, p.wait_limit));
+        if (!ok) break;
+        tg::tc_fence_after();
+        mma_tile_ts<D>(tmem + C::kColAcc0, tmem + C::dp_col(jp), dr0_mn + 2 * sp * kTile16, idesc_acc,
+                       jp == 0);   // dQ
+        tg::mma_commit_elect(dq_done);
+        tg::mma_commit_elect(&ring_empty[sp]);
       }
-      tg::tc_fence_after();
-      mma_tile_ts<D>(tmem + C::kColAcc0, tmem + C::kColDP, dr0_mn + k_off, idesc_acc, j == 0);   // dQ
-      tg::mma_commit_elect(dq_done);
-      tg::mma_commit_elect(&ring_empty[s]);
     }
     if (ok) tg::mma_commit_elect(acc_final);
     if (lane == 0) flags[2] = consumed;
@@ -700,21 +758,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int slot = j & 1;
+      const uint32_t dpc = C::dp_col(j);
       bool w = tg::mbar_wait(st_full, j & 1, vabort, p.wait_limit);
       w = w && tg::mbar_wait(&col_full[slot], (j >> 1) & 1, vabort, p.wait_limit);
       ok = barrier_all(1, 256, w);
       if (!ok) break;
       tg::tc_fence_after();
+      uint32_t pv[2][32];
+      tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + 64 * hh, pv[0]);
+      tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + 64 * hh + 32, pv[1]);
+      tg::tmem_ld_wait();
+      tg::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tg::mbar_arrive(s_free);  // S(j) is in registers: S(j + 1) may overwrite it
       const float *bias = sCols + slot * 256;
       const bool diag = j == qt;
       const uint64_t c2x = f2(c2, c2), chx = f2(ch, ch), nlx = f2(negl, negl), ndx = f2(-dd, -dd);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int c0 = 64 * hh + 32 * chunk;
-        uint32_t sv[32], dpv[32], xk[16];
-        tg::tmem_ld_32x32b_x32(lane_addr + C::kColS + c0, sv);
-        tg::tmem_ld_32x32b_x32(lane_addr + C::kColDP + c0, dpv);
-        tg::tmem_ld_wait();
+        uint32_t *sv = pv[chunk];
+        uint32_t dpv[32], xk[16];
+        tg::tmem_ld_32x32b_x32(lane_addr + dpc + c0, dpv);  // lands while P is computed
         const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
@@ -738,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c)
             if (c0 + c > r) sv[c] = 0u;
         }
+        tg::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float s0, s1;
@@ -746,13 +812,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                           chx), s0, s1);
           xk[c / 2] = tg::pack_bf16x2(s0, s1);
         }
-        tg::tmem_st_32x32b_x16(lane_addr + C::kColDP + 64 * hh + 16 * chunk, xk);
+        tg::tmem_st_32x32b_x16(lane_addr + dpc + 64 * hh + 16 * chunk, xk);
       }
       tg::tmem_st_wait();
       tg::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        tg::mbar_arrive(p_full);
+        tg::mbar_arrive(&p_full[j & 1]);
         tg::mbar_arrive(&col_empty[slot]);
       }
     }
