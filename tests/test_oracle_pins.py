@@ -5,9 +5,11 @@ closed form worked by hand (tests/golden/), a brute-force count, or an
 invariant the TokenGate pages fix. The planted-mistake tests at the end show
 that a dropped term, a flipped sign or a wrong head index fails a pin.
 """
+import inspect
 import json
 import math
 import os
+import textwrap
 
 import numpy as np
 import pytest
@@ -818,3 +820,170 @@ def test_gate_score_grad_per_head_by_finite_differences():
         up[j, c] += 1e-6
         dn[j, c] -= 1e-6
         assert abs((loss(up) - loss(dn)) / 2e-6 - ds[kept[j], c]) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Planted slips in the oracle's own source: each edit below makes one plausible mistake
+# in a copy of an oracle function (a dropped term, a transposed operand, a wrong axis,
+# sign or scale), and the pin that guards that function must reject the copy. The
+# unedited function passes the same check, so the pin, not the harness, tells them apart.
+# ---------------------------------------------------------------------------
+
+def _planted_oracle(fn, edits):
+    """fn with each (old, new) edit applied to its source (old found exactly once), compiled
+    in the oracle module's namespace."""
+    src = textwrap.dedent(inspect.getsource(fn))
+    for old, new in edits:
+        assert src.count(old) == 1, old
+        src = src.replace(old, new)
+    ns = dict(vars(O))
+    exec(compile(src, f"<planted {fn.__name__}>", "exec"), ns)
+    return ns[fn.__name__]
+
+
+def _close_all(got, refs, rtol, atol):
+    return all(np.allclose(a, r, rtol=rtol, atol=atol) for a, r in zip(got, refs))
+
+
+_BWD_SLIPS = {
+    "row_dot_dropped": [("dX = P * (dP - D)", "dX = P * dP")],
+    "row_dot_without_P": [("D = np.sum(do * o, axis=1, keepdims=True)", "D = np.sum(dP, axis=1, keepdims=True)")],
+    "dV_untransposed": [("dV[a:e, kv] += P.T @ do", "dV[a:e, kv] += P @ do")],
+    "dK_unscaled": [("dK[a:e, kv] += float(tau[h]) * c * (dX.T @ q)", "dK[a:e, kv] += float(tau[h]) * (dX.T @ q)")],
+    "dQ_transposed": [("dQ[a:e, h] = float(tau[h]) * c * (dX @ k)", "dQ[a:e, h] = float(tau[h]) * c * (dX.T @ k)")],
+    "dbias_over_queries": [("dbias[a:e, h] = dX.sum(axis=0)", "dbias[a:e, h] = dX.sum(axis=1)")],
+    "kv_head_modulo": [("kv = h // group", "kv = h % H_kv")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_BWD_SLIPS))
+def test_planted_backward_slips_fail_the_autograd_pin(kind):
+    Q, K, V, g, cu, tau, beta = _rand_attn(51, (9, 1, 14))
+    dO = np.random.default_rng(52).standard_normal(Q.shape)
+    out, (q, k, v, bias) = _torch_forward(Q, K, V, g, cu, tau, beta)
+    (out * torch.from_numpy(dO)).sum().backward()
+    refs = [t.grad.numpy() for t in (q, k, v, bias)]
+    assert _close_all(O.gated_attention_bwd(Q, K, V, g, dO, cu, tau, beta), refs, 1e-10, 1e-12)
+    bad = _planted_oracle(O.gated_attention_bwd, _BWD_SLIPS[kind])
+    assert not _close_all(bad(Q, K, V, g, dO, cu, tau, beta), refs, 1e-10, 1e-12)
+
+
+_SCORE_SLIPS = {
+    "silu_as_sigmoid": [("a = u / (1.0 + np.exp(-u))", "a = 1.0 / (1.0 + np.exp(-u))")],
+    "gate_sign": [("g = 1.0 / (1.0 + np.exp(-s))", "g = 1.0 / (1.0 + np.exp(s))")],
+    "instruction_gate_not_one": [("g = np.where(keep if g.ndim == 1 else keep[:, None], 1.0, g)", "g = g")],
+    "b1_dropped": [("u = u + np.asarray(b1, dtype=np.float64)[None, :]", "u = u")],
+    "b2_dropped": [("s = a @ w2 + float(b2)", "s = a @ w2")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_SCORE_SLIPS))
+def test_planted_gate_score_slips_fail_the_torch_pin(kind):
+    wl = I.WORKLOADS["tiny"]
+    gi = I.make_gate_inputs(wl)
+    h, W1, w2 = (I.bf16_bits_to_f64(gi[k]) for k in ("h", "W1", "w2"))
+    b1, b2 = np.random.default_rng(5).standard_normal(wl.d_g), 0.3
+    ref_s = F.linear(F.silu(F.linear(torch.from_numpy(h), torch.from_numpy(W1), torch.from_numpy(b1))),
+                     torch.from_numpy(w2)[None, :]).squeeze(1) + b2
+    ref_g = torch.sigmoid(ref_s)
+    ref_g[torch.from_numpy(gi["instr_mask"].astype(bool))] = 1.0
+    refs = (ref_s.numpy(), ref_g.numpy())
+    assert _close_all(O.gate_score(h, W1, w2, gi["instr_mask"], b1, b2), refs, 1e-12, 1e-12)
+    bad = _planted_oracle(O.gate_score, _SCORE_SLIPS[kind])
+    assert not _close_all(bad(h, W1, w2, gi["instr_mask"], b1, b2), refs, 1e-12, 1e-12)
+
+
+_NORM_SLIPS = {
+    "rms_over_every_row": [("doc = [j for j in range(a, e) if instr_mask[j] == 0]", "doc = list(range(a, e))")],
+    "variance_not_rooted": [("b[j] = s[j] / math.sqrt(ms + eps)", "b[j] = s[j] / (ms + eps)")],
+    "mean_absolute_value": [("ms = sum(s[j] * s[j] for j in doc) / len(doc)", "ms = sum(abs(s[j]) for j in doc) / len(doc)")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_NORM_SLIPS))
+def test_planted_normalisation_slips_fail_the_closed_form(kind):
+    fx = _golden("normalized_scores_closed_form.json")
+    args = (np.array(fx["s"]), np.array(fx["instr_mask"]), fx["cu_seqlens"])
+    assert np.allclose(O.normalize_scores(*args, eps=0.0), fx["b"], rtol=0, atol=1e-15)
+    bad = _planted_oracle(O.normalize_scores, _NORM_SLIPS[kind])
+    assert not np.allclose(bad(*args, eps=0.0), fx["b"], rtol=0, atol=1e-15)
+
+
+_GRAD_SLIPS = {
+    "sigmoid_factor_dropped": [("ds[kept_idx] = (dbias @ beta) * (1.0 - g_kept)", "ds[kept_idx] = dbias @ beta")],
+    "factor_g_not_one_minus_g": [("ds[kept_idx] = (dbias @ beta) * (1.0 - g_kept)", "ds[kept_idx] = (dbias @ beta) * g_kept")],
+    "beta_dropped": [("ds[kept_idx] = (dbias @ beta) * (1.0 - g_kept)", "ds[kept_idx] = dbias.sum(axis=1) * (1.0 - g_kept)")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_GRAD_SLIPS))
+def test_planted_score_gradient_slips_fail_finite_differences(kind):
+    Q, K, V, _, cu, tau, beta = _rand_attn(55, (10,))
+    rng = np.random.default_rng(56)
+    s = rng.standard_normal(10)
+    sig = lambda x: 1.0 / (1.0 + np.exp(-x))
+    dO = rng.standard_normal(Q.shape)
+    _, _, _, dbias = O.gated_attention_bwd(Q, K, V, sig(s), dO, cu, tau, beta)
+    kept = np.arange(10) * 2
+    loss = lambda ss: float(np.sum(dO * O.gated_attention(Q, K, V, sig(ss), cu, tau, beta)))
+    fd = []
+    for j in range(10):
+        up, dn = s.copy(), s.copy()
+        up[j] += 1e-6
+        dn[j] -= 1e-6
+        fd.append((loss(up) - loss(dn)) / 2e-6)
+    matches = lambda ds: np.allclose(ds[kept], fd, rtol=0, atol=1e-6)
+    assert matches(O.gate_score_grad(dbias, beta, sig(s), kept, 20))
+    assert not matches(_planted_oracle(O.gate_score_grad, _GRAD_SLIPS[kind])(dbias, beta, sig(s), kept, 20))
+
+
+_ROPE_SLIPS = {
+    "rotation_sign": [("x1 * c - x2 * s", "x1 * c + x2 * s")],
+    "frequency_exponent": [("theta ** (-2.0 * i / d_h)", "theta ** (-1.0 * i / d_h)")],
+    "interleaved_pairs": [("x1 = X[..., :half]", "x1 = X[..., 0::2]"), ("x2 = X[..., half:]", "x2 = X[..., 1::2]")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_ROPE_SLIPS))
+def test_planted_rope_slips_fail_the_complex_rotation(kind):
+    rng = np.random.default_rng(19)
+    X = rng.standard_normal((7, 3, 8))
+    pos = rng.integers(0, 5000, 7)
+    z = X[..., :4] + 1j * X[..., 4:]
+    zr = z * np.exp(1j * pos[:, None, None] * (1.0e6 ** (-np.arange(4) * 2.0 / 8))[None, None, :])
+    ref = np.concatenate([zr.real, zr.imag], axis=-1)
+    assert np.allclose(O.apply_rope(X, pos, 1.0e6), ref, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(_planted_oracle(O.apply_rope, _ROPE_SLIPS[kind])(X, pos, 1.0e6), ref,
+                           rtol=1e-12, atol=1e-12)
+
+
+_LSE_SLIPS = {
+    "no_causal_mask": [("x = np.where(causal,", "x = np.where(np.ones_like(causal),")],
+    "bias_dropped": [("+ bias[None, :],", ",")],
+    "max_not_added_back": [("out[a:e, h][fin] = mx[fin] + np.log(", "out[a:e, h][fin] = np.log(")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_LSE_SLIPS))
+def test_planted_lse_slips_fail_torch_logsumexp(kind):
+    Q, K, V, g, cu, tau, beta = _rand_attn(57, (6, 11))
+    ref = np.full((Q.shape[0], Q.shape[1]), np.nan)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        for h in range(Q.shape[1]):
+            z = torch.from_numpy(Q[a:e, h] @ K[a:e, h // 2].T) * (tau[h] / math.sqrt(Q.shape[2]))
+            z = z + beta[h] * torch.log(torch.from_numpy(g[a:e]))[None, :]
+            z = z.masked_fill(torch.ones(e - a, e - a, dtype=torch.bool).triu(1), float("-inf"))
+            ref[a:e, h] = torch.logsumexp(z, dim=1).numpy()
+    assert np.allclose(O.gated_attention_lse(Q, K, g, cu, tau, beta), ref, rtol=1e-12, atol=1e-12)
+    bad = _planted_oracle(O.gated_attention_lse, _LSE_SLIPS[kind])
+    assert not np.allclose(bad(Q, K, g, cu, tau, beta), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_planted_aggregation_slip_fails_the_mean_head_pin():
+    wl, gi, h, W1, W2, b1, b2 = _heads_case(4, seed=62)
+    s, _ = O.gate_score(h, W1, W2, gi["instr_mask"], b1, b2)
+    s1, _ = O.gate_score(h, W1, W2.mean(axis=0), gi["instr_mask"], b1, float(b2.mean()))
+    assert np.allclose(O.aggregate_heads(s), s1, rtol=1e-12, atol=1e-12)
+    bad = _planted_oracle(O.aggregate_heads, [("s.mean(axis=1)", "s.sum(axis=1)")])
+    assert not np.allclose(bad(s), s1, rtol=1e-12, atol=1e-12)
