@@ -987,3 +987,64 @@ def test_planted_aggregation_slip_fails_the_mean_head_pin():
     assert np.allclose(O.aggregate_heads(s), s1, rtol=1e-12, atol=1e-12)
     bad = _planted_oracle(O.aggregate_heads, [("s.mean(axis=1)", "s.sum(axis=1)")])
     assert not np.allclose(bad(s), s1, rtol=1e-12, atol=1e-12)
+
+
+_SELECT_SLIPS = {
+    "budget_counts_instruction_rows": [("K_b = min(K, len(prunable))",
+                                        "K_b = max(0, min(K - len(keep_always), len(prunable)))")],
+    "instruction_rows_dropped": [("keep = sorted(selected + keep_always)", "keep = sorted(selected)")],
+    "kept_in_score_order": [("keep = sorted(selected + keep_always)", "keep = selected + sorted(keep_always)")],
+    "smallest_scores_kept": [("return (0, -(x + 0.0))", "return (0, x + 0.0)")],
+    "negative_zero_below_zero": [("return (0, -(x + 0.0))", "return (0, -x, math.copysign(1.0, x) < 0)")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_SELECT_SLIPS))
+def test_planted_selection_slips_fail_brute_force(kind):
+    # every budget from 0 to one past the largest document count, on every tiny case
+    def agrees(select):
+        for s, mask, cu in _tiny_select_cases():
+            max_doc = max(int(np.sum(mask[cu[b]:cu[b + 1]] == 0)) for b in range(len(cu) - 1))
+            for K in range(0, max_doc + 2):
+                kept, cu_k = select(s, mask, cu, K)
+                ref, ref_cu = _brute_force_keep(s, mask, cu, K)
+                if kept.tolist() != ref.tolist() or cu_k.tolist() != ref_cu.tolist():
+                    return False
+        return True
+    assert agrees(O.topk_select)
+    fn = O._rank_key if kind in ("smallest_scores_kept", "negative_zero_below_zero") else O.topk_select
+    bad = _planted_oracle(fn, _SELECT_SLIPS[kind])
+    if fn is O._rank_key:  # the key function is a helper: select with the planted key in place
+        ns = dict(vars(O))
+        ns["_rank_key"] = bad
+        exec(compile(textwrap.dedent(inspect.getsource(O.topk_select)), "<planted topk_select>", "exec"), ns)
+        bad = ns["topk_select"]
+    assert not agrees(bad)
+
+
+_GATHER_SLIPS = {
+    "positions_from_zero_over_the_batch": [
+        ("p_k = (kept_idx - np.asarray(cu_seqlens, dtype=np.int64)[seq_of]).astype(np.int32)",
+         "p_k = kept_idx.astype(np.int32)")],
+    "positions_of_the_kept_list": [
+        ("p_k = (kept_idx - np.asarray(cu_seqlens, dtype=np.int64)[seq_of]).astype(np.int32)",
+         "p_k = np.arange(len(kept_idx), dtype=np.int32)")],
+    "gate_values_not_gathered": [("g_k = np.asarray(g)[kept_idx]", "g_k = np.asarray(g)[:len(kept_idx)]")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_GATHER_SLIPS))
+def test_planted_gather_slips_fail_the_original_id_pin(kind):
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(20, 30), instr_lens=(4, 6))
+    cu = I.cu_seqlens_of(wl.seq_lens)
+    rng = np.random.default_rng(3)
+    kept = np.sort(rng.choice(wl.T_total, size=25, replace=False)).astype(np.int32)
+    h = rng.standard_normal((wl.T_total, 8))
+    g = rng.random(wl.T_total)
+    want_pos = [j if j < cu[1] else j - cu[1] for j in kept]
+
+    def agrees(gather):
+        hk, pk, gk = gather(h, None, g, kept, cu)
+        return (pk.tolist() == want_pos and np.array_equal(hk, h[kept]) and np.array_equal(gk, g[kept]))
+    assert agrees(O.gather_kept)
+    assert not agrees(_planted_oracle(O.gather_kept, _GATHER_SLIPS[kind]))
