@@ -1048,3 +1048,31 @@ def test_planted_gather_slips_fail_the_original_id_pin(kind):
         return (pk.tolist() == want_pos and np.array_equal(hk, h[kept]) and np.array_equal(gk, g[kept]))
     assert agrees(O.gather_kept)
     assert not agrees(_planted_oracle(O.gather_kept, _GATHER_SLIPS[kind]))
+
+
+_TWO_BUDGET_SLIPS = {
+    "pruned_offsets_not_shifted": [('T + prune["cu_kept"][1:]', 'prune["cu_kept"][1:]')],
+    "pruned_half_first": [('cat = lambda k: np.concatenate([full[k], prune[k]])',
+                           'cat = lambda k: np.concatenate([prune[k], full[k]])')],
+    "full_budget_of_one_sequence": [("cu_seqlens, len(instr_mask), b1, b2)",
+                                     "cu_seqlens, int(cu_seqlens[1] - cu_seqlens[0]) // 2, b1, b2)")],
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_TWO_BUDGET_SLIPS))
+def test_planted_two_budget_slips_fail_the_pack_invariants(kind):
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(50, 0, 33), instr_lens=(4, 2, 6), d=64, d_g=32)
+    gi = I.make_gate_inputs(wl)
+    h = I.bf16_bits_to_f64(gi["h"])
+    W1, w2 = I.bf16_bits_to_f64(gi["W1"]), I.bf16_bits_to_f64(gi["w2"])
+    T, B = wl.T_total, wl.B
+
+    def agrees(pack):
+        out = pack(h, gi["pos"], W1, w2, gi["instr_mask"], gi["cu_seqlens"], 7)
+        cu = out["cu_packed"]
+        return (out["kept_idx"][:T].tolist() == list(range(T))
+                and cu[:B + 1].tolist() == gi["cu_seqlens"].tolist()
+                and all(cu[B + b + 1] - cu[B + b] == min(7, wl.doc_lens[b]) + wl.instr_lens[b] for b in range(B))
+                and np.array_equal(out["h_kept"], h[out["kept_idx"]]))
+    assert agrees(O.two_budget_prune_layer)
+    assert not agrees(_planted_oracle(O.two_budget_prune_layer, _TWO_BUDGET_SLIPS[kind]))
