@@ -79,8 +79,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 def _ptr(t) -> Optional[int]:
+    """Device address of a dense CUDA tensor (the C ABI takes no strides); None stays None.
+    A host tensor or a strided view would reach a kernel as a wrong address, so both raise."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(t.shape)} with strides {tuple(t.stride())}")
     return t.data_ptr()
 
 

@@ -195,3 +195,26 @@ def test_prune_layer_entry_points_reject_bad_arguments(lib):
         p, None, None, p, 1, 128, 256, p, None, p, 0.0, 64, 8, p, p, p, capacity, p, p, None, None, None, None)
     assert two(127) == binding.TG_ERR_INVALID_ARG                 # the full half alone is T_total rows
     assert lib.tg_read_device_status(None, None, None) == binding.TG_ERR_INVALID_ARG
+
+
+def test_binding_passes_only_dense_cuda_tensors():
+    import torch
+
+    class _Strided:  # stands in for a CUDA view with gaps between its elements
+        is_cuda = True
+        shape = (4, 2)
+
+        def is_contiguous(self):
+            return False
+
+        def stride(self):
+            return (4, 1)
+
+    assert binding._ptr(None) is None
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding._ptr(torch.zeros(4))                   # host memory is never handed to a kernel
+    with pytest.raises(ValueError, match="contiguous"):
+        binding._ptr(_Strided())
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.gate_score(torch.zeros(8, 256, dtype=torch.int16), torch.zeros(64, 256, dtype=torch.int16),
+                           torch.zeros(64, dtype=torch.int16), torch.zeros(8))
