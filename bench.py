@@ -414,10 +414,13 @@ def oracle_sample_step(wl, K, frac, cache):
     return est, t3 - t0
 
 
-def cpu_baseline(wl, K, frac, budget_s=20.0):
+def cpu_baseline(wl, K, frac, min_s=10.0, budget_s=30.0):
+    """The oracle as it stands, on repeated bounded samples of one step: at least min_s seconds
+    of CPU work and at least three samples, stopping once budget_s is spent; the median
+    estimate of the full step gives the value."""
     cache = {}
     ests, spent = [], 0.0
-    while spent < budget_s and len(ests) < 3:
+    while (spent < min_s or len(ests) < 3) and spent < budget_s:
         e, s = oracle_sample_step(wl, K, frac, cache)
         ests.append(e)
         spent += s
