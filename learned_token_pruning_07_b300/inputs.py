@@ -25,10 +25,15 @@ import numpy as np
 # ---------------------------------------------------------------------------
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round fp32 values to bf16 (round to nearest, ties to even); return uint16 bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    """Round fp32 values to bf16 (round to nearest, ties to even); return uint16 bits.
+    A NaN stays a NaN (quiet, same sign): rounding its payload could carry into +-inf."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
     rounding = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
-    return ((u + rounding) >> np.uint64(16)).astype(np.uint16)
+    out = ((u + rounding) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(f)
+    out[nan] = ((u[nan] >> np.uint64(16)) | np.uint64(0x0040)).astype(np.uint16)
+    return out
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

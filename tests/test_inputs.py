@@ -18,6 +18,19 @@ def test_bf16_rounding_matches_torch():
     assert np.array_equal(back, torch.from_numpy(x).to(torch.bfloat16).float().numpy())
 
 
+def test_bf16_rounding_of_special_values():
+    special = np.array([np.inf, -np.inf, 3.4e38, -3.4e38, 1e-40, -1e-45], np.float32)
+    ours = I.f32_to_bf16_bits(special)
+    ref = torch.from_numpy(special).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)                  # infinities, overflow to inf, subnormals
+    # NaNs stay NaN with their sign, including the signalling ones whose payload sits in the
+    # low 16 bits (adding the rounding bias to those would carry into the infinity pattern)
+    nans = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF800001, 0x7FBFFFFF], np.uint32).view(np.float32)
+    out = I.f32_to_bf16_bits(nans)
+    assert np.all(np.isnan(I.bf16_bits_to_f32(out)))
+    assert [int(v) >> 15 for v in out] == [0, 1, 0, 1, 0]
+
+
 def test_generators_are_deterministic_and_shaped():
     wl = I.WORKLOADS["tiny"]
     a, b = I.make_gate_inputs(wl), I.make_gate_inputs(wl)
