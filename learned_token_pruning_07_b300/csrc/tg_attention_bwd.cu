@@ -22,6 +22,9 @@
 //   3. bwd_dq_kernel: one CTA per (128-query tile, query head). It loops over the key tiles at or
 //      before its query tile: S = Q K^T, dP = dO V^T, dX as above (thread = query), and
 //      dQ += (c_h dX) K.
+// Both tensor-core passes are software-pipelined: the products of the next tile start as soon
+// as the elementwise warps have released the tensor-memory columns they overwrite, so they
+// run while the current tile's elementwise step is still working.
 // Every output element is written by exactly one CTA after sums in a fixed order: the results
 // are deterministic, with no atomics.
 //
