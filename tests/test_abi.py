@@ -218,3 +218,32 @@ def test_binding_passes_only_dense_cuda_tensors():
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.gate_score(torch.zeros(8, 256, dtype=torch.int16), torch.zeros(64, 256, dtype=torch.int16),
                            torch.zeros(64, dtype=torch.int16), torch.zeros(8))
+
+
+def _declared_params():
+    """name -> [parameter C type] for every TG_API declaration in the header."""
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"TG_API\s+[\w\s\*]+?\b(tg_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",")]
+        if params == ["void"]:
+            params = []
+        # drop the parameter name: the type is everything before the last identifier
+        out[m.group(1)] = [re.sub(r"\s*\b\w+\s*$", "", p).replace(" ", "") for p in params]
+    return out
+
+
+def _ctype_of(c_type):
+    if c_type.endswith("*") or c_type == "tg_stream_t":
+        return ctypes.c_void_p
+    return {"int32_t": ctypes.c_int32, "tg_status": ctypes.c_int32, "float": ctypes.c_float,
+            "uint64_t": ctypes.c_uint64}[c_type]
+
+
+def test_binding_argument_types_match_the_header():
+    # a parameter added, dropped or retyped on one side only would pass the wrong bytes
+    decls = _declared_params()
+    assert set(decls) == set(binding.SIGNATURES)
+    for name, c_params in decls.items():
+        _, argtypes = binding.SIGNATURES[name]
+        assert [_ctype_of(t) for t in c_params] == list(argtypes), name
