@@ -74,3 +74,34 @@ def test_peaks_come_from_the_measured_file_when_present():
         j = json.load(fh)
     assert p["source"] == "measured"
     assert p["hbm_gbs"] == float(j["hbm_gbs"]) and p["bf16_tflops"] == float(j["bf16_tflops"])
+
+
+def _run_bench(*args, env_extra=None):
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args], capture_output=True,
+                       text=True, env=env, timeout=300, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [ln for ln in r.stdout.splitlines() if ln.strip()]
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the reference arm times the oracle on the host cores; the tiny workload keeps this quick
+    line = json.loads(_run_bench("--impl", "reference", "--steps", "2", "--warmup", "3", "--workload", "tiny")[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 1
+    assert line["steps"] == 2 and line["warmup"] >= 3
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["ms_per_step"] == pytest.approx(1000.0 * 512 / line["value"], rel=1e-9)
+    assert line["config"]["workload"].startswith("tiny") and line["vs_baseline"] is None
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"] and cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_only_on_rank_zero():
+    out = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "tiny",
+                     env_extra={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert out == []
