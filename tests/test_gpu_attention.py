@@ -89,6 +89,12 @@ def test_attention_mha_group_of_one():
     _assert_close(*_run(wl, [200, 70]))
 
 
+def test_attention_at_the_largest_head_count():
+    # 128 query heads, the most the call takes, over 64 kv heads of 64
+    wl = I.with_changes(I.WORKLOADS["tiny"], H_q=128, H_kv=64)
+    _assert_close(*_run(wl, [70, 130]))
+
+
 def test_attention_sweep_k4096_full():
     wl = I.WORKLOADS["sweep_32k"]
     _assert_close(*_run(wl, [4096 + 256]))

@@ -128,6 +128,11 @@ def test_backward_mha_and_odd_group():
     _case(I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=6, H_kv=2), [130, 70], seed=22)
 
 
+def test_backward_at_the_largest_head_count():
+    # 128 query heads, the most the call takes, over 64 kv heads of 64
+    _case(I.with_changes(I.WORKLOADS["tiny"], H_q=128, H_kv=64), [70, 130], seed=23)
+
+
 def test_backward_is_deterministic():
     # every output element is written once after a fixed-order sum: two runs agree bit for bit
     wl = I.WORKLOADS["qwen3_1p7b_8k"]
