@@ -2,10 +2,10 @@
 //
 //   u = W1 h_j (+ b1),  s_j = w2 . SiLU(u) (+ b2),  g_j = sigmoid(s_j)  (g = 1 on non-prunable rows)
 //
-// Persistent kernel: one CTA per SM; CTAs run in clusters of two that walk pairs of
-// neighbouring 128-row tiles of h in lockstep. Each CTA of a pair loads its own h tile and
-// HALF of every W1 stage, multicasting that half into both CTAs, so each SM pulls half the
-// W1 bytes through L2 (W1 is re-read for every tile: without sharing it is 4x the h bytes). The d_g-wide hidden layer of a tile is computed as n_items column
+// Persistent kernel: one CTA per SM, each walking 128-row tiles of h (tile = blockIdx.x +
+// k * gridDim.x). Every CTA stages its own h tile and its own W1 slice through TMA; no CTA
+// reads another's shared memory or signals another's barriers. The d_g-wide hidden layer of a
+// tile is computed as n_items column
 // slices of at most 256 (two slices of 256 at d_g = 512). Each slice is one work item: a
 // d-reduction u_slice = h_tile W1_slice^T on the tensor cores (tcgen05.mma kind::f16, bf16
 // operands staged by TMA into 128-byte-swizzled shared memory, fp32 accumulator in one of
@@ -31,7 +31,6 @@ constexpr int kThreadsNorm = 320;  // + warps 6-9: row sums of squares for the f
 constexpr int kMaxDg = 512;
 constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
-constexpr int kPair = 2;  // CTAs of a cluster: neighbouring row tiles that share each W1 stage
 constexpr int kMaxGateHeads = 16;
 
 struct ScoreParams {
@@ -70,36 +69,8 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   return L;
 }
 
-// TMA tile load of W1 rows that lands at the same shared-memory offset in every CTA of the
-// pair and signals the barrier at the same offset in each (cluster multicast).
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                                 int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(tg::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(tg::smem_u32(bar)), "r"(x), "r"(y),
-      "h"(static_cast<uint16_t>((1u << kPair) - 1u))
-      : "memory");
-}
-
-// Arrive once on the barrier at this offset in both CTAs of the pair when every MMA issued so
-// far by the warp's elected lane has completed.
-__device__ __forceinline__ void mma_commit_pair_elect(uint64_t *bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(tg::smem_u32(bar)),
-      "h"(static_cast<uint16_t>((1u << kPair) - 1u))
-      : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 template <bool NORM, int GHP>
-__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
+__global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -130,8 +101,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       tg::mbar_init(&full[i], 1);
-      // one MMA commit from each CTA of the pair (+ this CTA's four norm warps)
-      tg::mbar_init(&empty[i], kPair + (NORM ? 4 : 0));
+      // one MMA commit (+ this CTA's four norm warps)
+      tg::mbar_init(&empty[i], 1 + (NORM ? 4 : 0));
     }
     for (int i = 0; i < 2; ++i) {
       tg::mbar_init(&acc_full[i], 1);
@@ -169,27 +140,20 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
   tg::tc_fence_before();
-  cluster_sync_all();  // both CTAs' barriers are initialised before any multicast arrives
+  __syncthreads();
   tg::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int32_t *vabort = abort_flag;
   const uint32_t stage_bytes = L.a_bytes + L.b_bytes;
-  // the pair (cluster) walks tile pairs in lockstep; this CTA owns tile 2 * pair + rank
-  uint32_t rank;
-  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  const int pair0 = blockIdx.x / kPair;
-  const int pair_stride = gridDim.x / kPair;
-  const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
-  const int half_n = p.item_n / kPair;  // W1 rows of a stage this CTA loads for both
+  const int tile0 = blockIdx.x;
+  const int tile_stride = gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer: stage = h tile [128 x 64] + W1 slice [item_n x 64] ----
       int kc = 0;
       bool ok = !p.withhold;
-      for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
-        // a tile past the end (odd tile count) re-reads the last tile; its rows are not stored
-        const int tile = min(pr * kPair + static_cast<int>(rank), p.n_tiles - 1);
+      for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
         for (int item = 0; item < p.n_items && ok; ++item) {
           for (int kt = 0; kt < p.KT; ++kt, ++kc) {
             const int st = kc % kStages;
@@ -198,11 +162,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
               ok = false;
               break;
             }
-            // this stage receives: own h tile + both halves of the W1 slice (one from each CTA)
+            // this stage receives the h tile and the W1 slice, both for this CTA alone
             tg::mbar_arrive_expect_tx(&full[st], stage_bytes);
             tg::tma_load_2d(sA + st * L.a_bytes, &tm_h, &full[st], kt * kBK, tile * kBM);
-            tma_load_2d_pair(sB + st * L.b_bytes + rank * half_n * (kBK * 2), &tm_w, &full[st],
-                             kt * kBK, item * p.item_n + static_cast<int>(rank) * half_n);
+            tg::tma_load_2d(sB + st * L.b_bytes, &tm_w, &full[st], kt * kBK, item * p.item_n);
             *n_issued = kc + 1;
           }
         }
@@ -216,7 +179,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       const uint64_t b0 = tg::smem_desc(tg::smem_u32(sB), 16, 1024, tg::kSwz128);
       int kc = 0, it = 0;
       bool ok = true;
-      for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride) {
+      for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
         for (int item = 0; item < p.n_items && ok; ++item, ++it) {
           const int buf = it & 1;
           if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1u, vabort, p.wait_limit))) {
@@ -236,7 +199,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)  // a K-step of 16 is 32 bytes into the 128-byte row
               tg::mma_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
-            mma_commit_pair_elect(&empty[st]);  // the stage is free once both CTAs have read it
+            tg::mma_commit_elect(&empty[st]);  // the stage is free once these MMAs have read it
             if (lane == 0) *n_consumed = kc + 1;
           }
           if (ok) tg::mma_commit_elect(&acc_full[buf]);
@@ -257,8 +220,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0, ti = 0;
     bool ok = true;
-    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride, ++ti) {
-      const int tile = pr * kPair + static_cast<int>(rank);
+    for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
       float acc[GHP];
 #pragma unroll
       for (int c = 0; c < GHP; ++c) acc[c] = 0.0f;
@@ -361,7 +323,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     const int r = (warp - 6) * 32 + lane;
     int kc = 0, ti = 0;
     bool ok = true;
-    for (int pr = pair0; pr < n_pairs && ok; pr += pair_stride, ++ti) {
+    for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
       float sq = 0.0f;
       for (int item = 0; item < p.n_items && ok; ++item) {
         for (int kt = 0; kt < p.KT; ++kt, ++kc) {
@@ -414,8 +376,6 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     tg::tc_fence_after();
     tg::tmem_dealloc(tmem, kTmemCols);
   }
-  // neither CTA leaves while its peer may still signal its barriers or write its stages
-  cluster_sync_all();
 }
 
 }  // namespace
@@ -479,18 +439,17 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(d_g)};
     const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.item_n / kPair)};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.item_n)};
     if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
   const SmemLayout L = score_smem_layout(p.item_n, ghp);
-  const int n_pairs = (p.n_tiles + kPair - 1) / kPair;
-  int pairs = num_sms() / kPair;
-  if (pairs > n_pairs) pairs = n_pairs;
+  int ctas = num_sms();
+  if (ctas > p.n_tiles) ctas = p.n_tiles;
   auto kernel = rmsnorm ? score_kernel_for<true>(ghp) : score_kernel_for<false>(ghp);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
-  return record_cuda(launch_pdl(kernel, dim3(pairs * kPair), dim3(rmsnorm ? kThreadsNorm : kThreads),
+  return record_cuda(launch_pdl(kernel, dim3(ctas), dim3(rmsnorm ? kThreadsNorm : kThreads),
                                 L.total, stream, tm_h, tm_w, p));
 }
 
