@@ -199,6 +199,37 @@ TG_API tg_status tg_gated_attention(const uint16_t *Q, const uint16_t *K, const 
                              int32_t *status, tg_stream_t stream);
 
 /*
+ * tg_gated_attention_workspace_size — bytes of device workspace tg_gated_attention_ws needs for
+ *   this shape on the current device (0 when the launch would not split its key ranges).
+ *   Arguments as tg_gated_attention. Invalid shapes give 0.
+ */
+TG_API size_t tg_gated_attention_workspace_size(int32_t B, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                                int32_t d_h);
+
+/*
+ * tg_gated_attention_ws — tg_gated_attention (deep dive section 3.2, Eqs. (5) and (8)) with a
+ *   caller workspace, used when one CTA per 128-row query tile would leave SMs idle (short kept
+ *   sequences: small budgets K). Each query tile's causal key range is then cut into chunks of
+ *   key tiles, one CTA each; a chunk writes its unnormalised fp32 partial output and its row
+ *   statistics (reference max, sum of weights) to the workspace, and the last chunk of the tile
+ *   to finish adds the chunks' parts in chunk order (so the result does not depend on which
+ *   chunk finishes last) and writes O. Results match tg_gated_attention within rounding.
+ *   workspace [device] of workspace_bytes >= tg_gated_attention_workspace_size(...) for the
+ *     same B, max_seqlen, H_q, H_kv, d_h, 256-byte aligned; may be NULL (with 0 bytes) when
+ *     that size is 0. Its first bytes are arrival counters: the workspace must be zero-filled
+ *     before its first use, and every call that completes leaves them zero again. After a call
+ *     that reported TG_DEV_TIMEOUT, zero it again. Calls that share a workspace must not run
+ *     concurrently. Too small or misaligned: TG_ERR_INVALID_ARG.
+ *   Other arguments, layouts and errors as tg_gated_attention.
+ */
+TG_API tg_status tg_gated_attention_ws(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
+                                int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                void *workspace, size_t workspace_bytes, int32_t *status,
+                                tg_stream_t stream);
+
+/*
  * tg_gated_attention_lse — tg_gated_attention that also writes, for every kept row i and query
  *   head h, lse[i * H_q + h] = ln sum_{j <= i} exp(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j)
  *   (-inf when every key has zero weight): what the backward needs to rebuild P.

@@ -34,6 +34,9 @@ SIGNATURES = {
     "tg_gate_score_heads": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tg_gather_kept": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "tg_gated_attention": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_gated_attention_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "tg_gated_attention_ws": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t,
+                                   _P, _P]),
     "tg_gated_attention_lse": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tg_gated_attention_bwd": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _P, _P]),
@@ -178,17 +181,40 @@ def gather_kept(h, cu_seqlens, kept_idx, cu_kept, h_kept, pos=None, g=None, pos_
 
 
 def gated_attention(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, status=None,
-                    stream=None):
+                    stream=None, workspace=None):
+    """tg_gated_attention, or tg_gated_attention_ws when a workspace tensor is given (see
+    attention_workspace)."""
     M, H_q, d_h = Q.shape
     H_kv = K.shape[1]
     B = cu_kept.numel() - 1
     tau_a, tau_p = _host_f32(tau)
     beta_a, beta_p = _host_f32(beta)
-    st = load().tg_gated_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept), B, M,
-                                   int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O),
-                                   _ptr(status), _stream(stream))
+    if workspace is None:
+        st = load().tg_gated_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept), B, M,
+                                       int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O),
+                                       _ptr(status), _stream(stream))
+        name = "tg_gated_attention"
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        st = load().tg_gated_attention_ws(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept), B, M,
+                                          int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O),
+                                          _ptr(workspace) if nbytes else None, nbytes, _ptr(status),
+                                          _stream(stream))
+        name = "tg_gated_attention_ws"
     del tau_a, beta_a
-    _check("tg_gated_attention", st)
+    _check(name, st)
+
+
+def gated_attention_workspace_size(B: int, max_seqlen: int, H_q: int, H_kv: int, d_h: int) -> int:
+    return int(load().tg_gated_attention_workspace_size(int(B), int(max_seqlen), int(H_q), int(H_kv), int(d_h)))
+
+
+def attention_workspace(B: int, max_seqlen: int, H_q: int, H_kv: int, d_h: int, device="cuda"):
+    """A zero-filled workspace for gated_attention(..., workspace=...) of this shape (an empty
+    tensor when the launch does not split)."""
+    import torch
+    n = gated_attention_workspace_size(B, max_seqlen, H_q, H_kv, d_h)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def normalize_scores(s, cu_seqlens, b_out, instr_mask=None, eps: float = 1e-6, b_sel=None, status=None,

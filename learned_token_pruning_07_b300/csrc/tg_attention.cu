@@ -25,6 +25,8 @@
 // is rare; the result is exact either way because O and l share the same reference. The
 // softmax runs on packed fp32 pairs (fma/add .f32x2) with 3-input max, and only the diagonal
 // key tile carries the causal mask.
+#include <algorithm>
+
 #include "tg_common.cuh"
 
 namespace {
@@ -34,6 +36,11 @@ constexpr int kBlockN = 128;      // keys per KV tile
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxHeads = 128;
+constexpr int kMaxChunkItems = 256;  // (query tile, key chunk) entries of a split launch
+constexpr int kMaxChunks = 3;        // chunks of one query tile in a split launch
+// Split only when the heaviest query tile walks at least this many key tiles: below that, the
+// extra arrival and combine (about two key steps) cost more than the shorter walk saves.
+constexpr int kMinSplitSteps = 6;
 
 template <int D>
 struct AttnCfg {
@@ -67,9 +74,38 @@ struct AttnParams {
   int32_t *status;
   uint64_t wait_limit, drain_limit;
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
+  // Split key range (a launch that would leave SMs idle): query tile tq's key tiles 0..tq are cut
+  // into chunks of `chunk` tiles, one CTA each. A chunk writes its unnormalised fp32 partial O
+  // and its (reference max, row sum) to a workspace slot; the last chunk of a tile to finish
+  // (an arrival counter per tile) combines the slots in chunk order and writes O. Each counter
+  // is reset to 0 by the combining CTA, so a workspace that starts zeroed stays reusable.
+  int32_t split;       // 0: one CTA per query tile
+  int32_t chunk;       // key tiles per chunk
+  int32_t n_u;         // (query tile, chunk) entries per (sequence, head pair)
+  int32_t *ws_count;   // [B * pairs * n_qt_max] arrival counters
+  float *ws_part;      // [B * pairs * n_u] slots of SlotFloats<D>() floats
+  uint32_t u_tab[kMaxChunkItems];  // entry -> tq | chunk index << 16, heaviest first
   float scale_log2[kMaxHeads];  // kLogGate: tau_h * log2(e) / sqrt(d_h); kEq8: temp_h
   float beta[kMaxHeads];        // kLogGate: beta_h; kEq8: gain_h * log2(e)
 };
+
+// One workspace slot of a split launch: O as [2 heads][D / 4 column blocks][128 rows] float4
+// (unnormalised fp32), then (m, l) as [2 heads][128 rows] float2.
+template <int D>
+__host__ __device__ constexpr size_t slot_floats() {
+  return static_cast<size_t>(2) * 128 * D + 2 * 128 * 2;
+}
+
+// Slots of query tiles 0..tq-1 (tile t has ceil((t + 1) / chunk) chunks).
+__host__ __device__ inline int chunk_slot_base(int tq, int chunk) {
+  int s = 0;
+  for (int t = 0; t < tq; ++t) s += (t + chunk) / chunk;
+  return s;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -77,11 +113,8 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// log2 of a gate value; a subnormal gate keeps its own weight g^beta (see tg::log2_gate)
+__device__ __forceinline__ float lg2(float x) { return tg::log2_gate(x); }
 
 // Packed fp32 pairs (Blackwell .f32x2 arithmetic).
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -113,7 +146,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gated_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -154,11 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hp = item % p.pairs;
   const int rest = item / p.pairs;
   const int b = rest % p.B;
-  const int tq = p.n_qt_max - 1 - rest / p.B;
+  int tq, chunk_id = 0;
+  if (SPLIT) {
+    const uint32_t e = p.u_tab[rest / p.B];
+    tq = static_cast<int>(e & 0xFFFFu);
+    chunk_id = static_cast<int>(e >> 16);
+  } else {
+    tq = p.n_qt_max - 1 - rest / p.B;
+  }
   int seq_start = p.cu_kept[b];
   int seq_end = p.cu_kept[b + 1];
   if (seq_start < 0 || seq_end < seq_start || seq_end - seq_start > p.max_seqlen) {
-    if (threadIdx.x == 0 && tq == p.n_qt_max - 1 && hp == 0) tg::report(p.status, TG_DEV_BAD_SEQLENS);
+    if (threadIdx.x == 0 && tq == p.n_qt_max - 1 && hp == 0 && chunk_id == 0) tg::report(p.status, TG_DEV_BAD_SEQLENS);
     return;
   }
   seq_start = min(seq_start, p.M_cap);
@@ -166,7 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seq_len = seq_end - seq_start;
   const int q0 = tq * kBlockM;
   if (q0 >= seq_len) return;  // uniform for the CTA
-  const int n_kv = tq + 1;    // causal: key tiles 0..tq
+  // causal: key tiles 0..tq, or this CTA's chunk j0 .. j0 + n_kv - 1 of them
+  const int j0 = SPLIT ? chunk_id * p.chunk : 0;
+  const int n_kv = SPLIT ? min(p.chunk, tq + 1 - j0) : tq + 1;
+  const int n_chunks = SPLIT ? (tq + p.chunk) / p.chunk : 1;
   const int h0 = hp * p.heads_per_cta;
   const int kvh = h0 / p.group;
   const int n_tiles = p.heads_per_cta;  // Q tiles in this CTA (1 or 2)
@@ -223,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTileBytes);
         for (int hf = 0; hf < C::kHalves; ++hf) {
           tg::tma_load_3d(sK + st * C::kTileBytes + hf * 16384, &tm_k, &kv_full[st], hf * 64, kvh,
-                          seq_start + j * kBlockN);
+                          seq_start + (j0 + j) * kBlockN);
           tg::tma_load_3d(sV + st * C::kTileBytes + hf * 16384, &tm_v, &kv_full[st], hf * 64, kvh,
-                          seq_start + j * kBlockN);
+                          seq_start + (j0 + j) * kBlockN);
         }
         issued = j + 1;
       }
@@ -336,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float pad = MODE == kEq8 ? 0.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int k = j * kBlockN + lane * 4 + i;
+          const int k = (j0 + j) * kBlockN + lane * 4 + i;
           const size_t row = static_cast<size_t>(seq_start + k) * p.g_cols;
           gv0[i] = k < seq_len ? p.g[row + col0] : pad;
           gv1[i] = col1 == col0 ? gv0[i] : (k < seq_len ? p.g[row + col1] : pad);
@@ -358,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - 4) >> 2;          // Q tile 0 (warps 4-7) or 1 (warps 8-11)
     const int wq = warp & 3;                 // TMEM lane quarter
     const int r = wq * 32 + lane;            // query row within the tile
+    float m_ref = -INFINITY;  // reference max (log2 units)
+    float l = 0.0f;           // row sum relative to it
     if (t < n_tiles) {
       const int h = h0 + t;
       const float scale = p.scale_log2[h];
@@ -380,8 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float s_mul = MODE == kEq8 ? (use_bias ? c1 : c1 * tau_row) : scale;
       const uint64_t scale2 = f2(s_mul, s_mul);
       const uint64_t tau2 = f2(tau_row, tau_row);
-      float m_ref = -INFINITY;  // reference max (log2 units)
-      float l = 0.0f;
       bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % C::kStages;
@@ -425,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             x[2 * c + 1] = __float_as_uint(a1);
           }
         }
-        if (j == tq) {
+        if (j0 + j == tq) {
           // diagonal tile: key c is visible to row r only when c <= r
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -436,10 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmax3(__uint_as_float(x[i]), __uint_as_float(x[8 + i]), __uint_as_float(x[16 + i]));
 #pragma unroll
-        for (int c = 24; c < 128; c += 16) {
+        for (int c = 24; c < 120; c += 16) {  // columns 24..119, two per chain per step
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(x[120 + i]));  // columns 120..127
         const float tile_max = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         // lazy max update; rescale O and l only when the max moved by more than the threshold
         float alpha = 1.0f;
@@ -488,9 +533,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tg::tc_fence_before();
         tg::mbar_arrive(&p_full[t]);
       }
-      // ---- epilogue: O / l -> bf16 rows of O ----
+      // ---- epilogue: O / l -> bf16 rows of O (or this chunk's partial row to its slot) ----
       if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&o_final[t], 0, vabort, p.wait_limit));
-      if (ok) {
+      if (SPLIT && ok && n_chunks > 1) {
+        tg::tc_fence_after();
+        // unnormalised fp32 O row and (reference max, row sum), both relative to m_use
+        const int row = q0 + r;
+        float *slot = p.ws_part + (static_cast<size_t>(b * p.pairs + hp) * p.n_u +
+                                   chunk_slot_base(tq, p.chunk) + chunk_id) * slot_floats<D>();
+        // column-block-major: float4 c4 of row r at [t][c4][r], so a warp's 32 rows are 512
+        // contiguous bytes for every store here and every load of the combine
+        float4 *opart = reinterpret_cast<float4 *>(slot) + static_cast<size_t>(t) * (D / 4) * 128 + r;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
+          tg::tmem_ld_wait();
+          if (row < seq_len) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              opart[(c0 / 4 + i) * 128] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          }
+        }
+        if (row < seq_len)
+          *reinterpret_cast<float2 *>(slot + static_cast<size_t>(2) * 128 * D + (t * 128 + r) * 2) =
+              make_float2((m_ref == -INFINITY) ? 0.0f : m_ref, l);
+      } else if (ok) {
         tg::tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
         const int row = q0 + r;
@@ -516,8 +584,139 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
-      } else {
-        *vabort = 1;
+      }
+      if (!ok) *vabort = 1;
+    }
+    if (SPLIT && n_chunks > 1) {
+      // ---- split key range: arrive; the last chunk of this query tile combines every slot ----
+      // All eight warps take part (warps of an absent second head included), so the named
+      // barrier always completes. A chunk that gave up still arrives, so the counter stays
+      // consistent; the status word then carries TG_DEV_TIMEOUT.
+      // The barrier orders every thread's partial stores before thread 128's release; its
+      // acq_rel add then publishes them device-wide with the arrival, and, for the last chunk,
+      // acquires every other chunk's published partial before the barrier below.
+      named_bar_sync(1, 256);
+      int32_t *s_last = abort_flag + 4;
+      if (threadIdx.x == 128) {
+        int32_t *cnt = p.ws_count + (static_cast<size_t>(b) * p.pairs + hp) * p.n_qt_max + tq;
+        int prev;
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
+        const int last = prev == n_chunks - 1;
+        if (last) *cnt = 0;  // ready for the next call on this workspace
+        *s_last = last;
+      }
+      named_bar_sync(1, 256);
+      const int row = q0 + r;
+      // warp-uniform condition: the tensor-memory loads below are warp-collective
+      if (*s_last && t < n_tiles) {
+        const bool valid = row < seq_len;
+        const int h = h0 + t;
+        const uint32_t colO = t == 0 ? C::kColO0 : C::kColO1;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float *slot0 = p.ws_part + (static_cast<size_t>(b * p.pairs + hp) * p.n_u +
+                                          chunk_slot_base(tq, p.chunk)) * slot_floats<D>();
+        const size_t ml_off = static_cast<size_t>(2) * 128 * D + (t * 128 + r) * 2;
+        const size_t o_off = static_cast<size_t>(t) * (D / 4) * 128 + r;  // in float4, then + c4 * 128
+        // This CTA's own chunk is read back from tensor memory and registers (the same values it
+        // stored). The other chunks' rows sit in L2, about a thousand cycles away, so each thread
+        // stages its own rows of them into the (now idle) operand buffers with asynchronous
+        // 16-byte copies, 32 columns per round and up to three rounds in flight (64 KB each, in
+        // the 192 KB of Q/K/V buffers; both rounds of d_h = 64 fit its 128 KB), and reads them back
+        // from shared memory: about one round trip instead of one per load round. Weights 2^(m_c - M) over
+        // the chunks with a non-empty sum; every sum runs in chunk order.
+        const int tl = threadIdx.x - 128;  // 0..255
+        constexpr int kRounds = D / 32;
+        constexpr int kBufs = kRounds < 3 ? kRounds : 3;
+        static_assert(kBufs * (kMaxChunks - 1) * 8 * 256 * 16 <= C::kOffBias, "staging fits the operand buffers");
+        float4 *stage = reinterpret_cast<float4 *>(smem);  // [kBufs][kMaxChunks - 1][8][256]
+        int rem[kMaxChunks - 1];
+        int n_rem = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c)
+          if (c < n_chunks && c != chunk_id && n_rem < kMaxChunks - 1) rem[n_rem++] = c;
+        auto issue_round = [&](int c0) {
+          float4 *dst = stage + ((c0 / 32) % kBufs) * (kMaxChunks - 1) * 8 * 256;
+          for (int k = 0; k < n_rem; ++k) {
+            const float4 *src = reinterpret_cast<const float4 *>(slot0 + rem[k] * slot_floats<D>()) + o_off + (c0 / 4) * 128;
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tg::smem_u32(dst + (k * 8 + i) * 256 + tl)),
+                             "l"(src + i * 128)
+                             : "memory");
+            }
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+#pragma unroll
+        for (int rr = 0; rr < kBufs; ++rr) issue_round(rr * 32);
+        float mc[kMaxChunks], lc[kMaxChunks];
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+          float2 ml = make_float2(0.0f, 0.0f);
+          if (c == chunk_id) ml = make_float2((m_ref == -INFINITY) ? 0.0f : m_ref, l);
+          else if (valid && c < n_chunks) ml = __ldcg(reinterpret_cast<const float2 *>(slot0 + c * slot_floats<D>() + ml_off));
+          mc[c] = ml.x;
+          lc[c] = ml.y;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c)
+          if (lc[c] > 0.0f) M = fmaxf(M, mc[c]);
+        float w[kMaxChunks], L = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+          w[c] = lc[c] > 0.0f ? ex2(mc[c] - M) : 0.0f;
+          L = fmaf(w[c], lc[c], L);
+        }
+        const float inv_L = L > 0.0f ? 1.0f / L : 0.0f;
+        if (p.lse != nullptr && valid)
+          p.lse[static_cast<size_t>(seq_start + row) * p.H_q + h] =
+              L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        uint16_t *orow = p.O + (static_cast<size_t>(seq_start + row) * p.H_q + h) * D;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          // round r has landed once at most the rounds issued after it are still in flight
+          const int pending = min(kBufs - 1, kRounds - 1 - c0 / 32);
+          if (pending >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+          else if (pending == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+          else asm volatile("cp.async.wait_group 0;" ::: "memory");
+          const float4 *src = stage + ((c0 / 32) % kBufs) * (kMaxChunks - 1) * 8 * 256;
+          uint32_t own[32];
+          tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, own);
+          tg::tmem_ld_wait();
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+          int k = 0;
+#pragma unroll
+          for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= n_chunks) break;
+            if (c == chunk_id) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = fmaf(w[c], __uint_as_float(own[i]), acc[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 x = src[(k * 8 + i) * 256 + tl];
+                acc[4 * i] = fmaf(w[c], x.x, acc[4 * i]);
+                acc[4 * i + 1] = fmaf(w[c], x.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(w[c], x.z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(w[c], x.w, acc[4 * i + 3]);
+              }
+              ++k;
+            }
+          }
+          if (valid) {
+            uint32_t wv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) wv[i] = tg::pack_bf16x2(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+          }
+          // this round's buffer is refilled by round r + kBufs
+          if (c0 + 32 * kBufs < D) issue_round(c0 + 32 * kBufs);
+        }
       }
     }
   }
@@ -564,15 +763,21 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
     if (!tg_host::encode_tmap_bf16(&tm_v, V, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(gated_attention_kernel<D, MODE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  // a split launch is its own instantiation, so the key loop of the one-CTA-per-tile kernel keeps
+  // its register allocation
+  auto kernel = gated_attention_kernel<D, MODE, false>;
+  if constexpr (MODE == kLogGate) {
+    if (p.split) kernel = gated_attention_kernel<D, MODE, true>;
+  } else {
+    if (p.split) return TG_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return tg_host::record_cuda(e);
-  const long long grid = static_cast<long long>(p.n_qt_max) * p.B * p.pairs;
+  const long long grid = static_cast<long long>(p.split ? p.n_u : p.n_qt_max) * p.B * p.pairs;
   if (grid == 0) return TG_OK;
   if (grid > 0x7FFFFFFFLL) return TG_ERR_UNSUPPORTED;
-  return tg_host::record_cuda(tg_host::launch_pdl(gated_attention_kernel<D, MODE>, dim3(static_cast<int>(grid)),
-                                                  dim3(kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, p));
+  return tg_host::record_cuda(tg_host::launch_pdl(kernel, dim3(static_cast<int>(grid)), dim3(kThreads),
+                                                  C::kSmemBytes, stream, tm_q, tm_k, tm_v, p));
 }
 
 }  // namespace
@@ -580,6 +785,49 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
 namespace tg_host {
 
 namespace {
+
+// How a launch splits its key ranges (see AttnParams): only when one CTA per query tile would
+// leave SMs idle. The chunk is the smallest number of key tiles for which every (query tile,
+// chunk) CTA still fits in one wave on this device, so the longest CTA is as short as it can be
+// without a second wave.
+struct SplitPlan {
+  int32_t split = 0, chunk = 0, n_u = 0;
+  uint32_t tab[kMaxChunkItems] = {};
+  size_t ws_bytes = 0;
+};
+
+size_t count_bytes(int32_t B, int32_t pairs, int32_t n_qt) {
+  const size_t n = static_cast<size_t>(B) * pairs * n_qt * sizeof(int32_t);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+SplitPlan plan_split(int32_t B, int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h, int sms) {
+  SplitPlan sp;
+  const int32_t group = H_q / H_kv;
+  const int32_t pairs = H_q / ((group % 2 == 0) ? 2 : 1);
+  const int32_t n_qt = (max_seqlen + kBlockM - 1) / kBlockM;
+  const long long base = static_cast<long long>(n_qt) * B * pairs;
+  if (n_qt < kMinSplitSteps || base >= sms) return sp;
+  // at most kMaxChunks chunks per query tile: the combine keeps one register set per chunk
+  for (int32_t chunk = (n_qt + kMaxChunks - 1) / kMaxChunks; chunk < n_qt; ++chunk) {
+    const int32_t n_u = chunk_slot_base(n_qt, chunk);
+    if (n_u > kMaxChunkItems) continue;
+    if (static_cast<long long>(n_u) * B * pairs > sms) continue;
+    sp.split = 1;
+    sp.chunk = chunk;
+    sp.n_u = n_u;
+    // heaviest first: by chunk length, then by query tile (later tiles see more keys)
+    int k = 0;
+    for (int32_t len = chunk; len >= 1; --len)
+      for (int32_t tq = n_qt - 1; tq >= 0; --tq)
+        for (int32_t c = 0; c * chunk <= tq; ++c)
+          if (std::min(chunk, tq + 1 - c * chunk) == len) sp.tab[k++] = static_cast<uint32_t>(tq) | (static_cast<uint32_t>(c) << 16);
+    const size_t slot = d_h == 128 ? slot_floats<128>() : slot_floats<64>();
+    sp.ws_bytes = count_bytes(B, pairs, n_qt) + static_cast<size_t>(B) * pairs * n_u * slot * sizeof(float);
+    return sp;
+  }
+  return sp;
+}
 
 AttnParams common_params(const float *bias_src, int32_t H_g, const int32_t *pos, const int32_t *cu_kept,
                          int32_t B, int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv, uint16_t *O,
@@ -605,19 +853,48 @@ AttnParams common_params(const float *bias_src, int32_t H_g, const int32_t *pos,
   p.wait_limit = wait_limit_ns();
   p.drain_limit = drain_limit_ns();
   p.withhold = (withhold_mask() & TG_WITHHOLD_ATTENTION) != 0;
+  p.split = 0;
+  p.chunk = 0;
+  p.n_u = 0;
+  p.ws_count = nullptr;
+  p.ws_part = nullptr;
   return p;
 }
 
+// Take the split plan when a workspace is given; a split launch needs plan.ws_bytes of it.
+tg_status apply_split(AttnParams &p, int32_t d_h, void *workspace, size_t workspace_bytes) {
+  if (workspace == nullptr) return TG_OK;
+  const SplitPlan sp = plan_split(p.B, p.max_seqlen, p.H_q, p.H_kv, d_h, num_sms());
+  if (!sp.split) return TG_OK;
+  if (workspace_bytes < sp.ws_bytes) return TG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TG_ERR_INVALID_ARG;
+  p.split = 1;
+  p.chunk = sp.chunk;
+  p.n_u = sp.n_u;
+  for (int i = 0; i < kMaxChunkItems; ++i) p.u_tab[i] = sp.tab[i];
+  p.ws_count = static_cast<int32_t *>(workspace);
+  p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + count_bytes(p.B, p.pairs, p.n_qt_max));
+  return TG_OK;
+}
+
 }  // namespace
+
+size_t gated_attention_workspace_size(int32_t B, int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h) {
+  if (B < 1 || max_seqlen < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || (d_h != 64 && d_h != 128)) return 0;
+  return plan_split(B, max_seqlen, H_q, H_kv, d_h, num_sms()).ws_bytes;
+}
 
 tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                                  const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
                                  int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
                                  int32_t d_h, const float *tau, const float *beta, uint16_t *O,
-                                 int32_t *status, cudaStream_t stream, float *lse) {
+                                 int32_t *status, cudaStream_t stream, float *lse, void *workspace,
+                                 size_t workspace_bytes) {
   if (M_cap == 0 || max_seqlen == 0) return TG_OK;
   AttnParams p = common_params(g, H_g, nullptr, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, O, status);
   p.lse = lse;
+  const tg_status st = apply_split(p, d_h, workspace, workspace_bytes);
+  if (st != TG_OK) return st;
   const float log2e = 1.4426950408889634f;
   for (int h = 0; h < kMaxHeads; ++h) {
     p.scale_log2[h] = h < H_q ? tau[h] * log2e / std::sqrt(static_cast<float>(d_h)) : 0.0f;

@@ -405,9 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a new query head: this key's bias beta_h log2 g_j and the logit scale
         bias2 = 0.0f;
         if (p.g != nullptr && p.beta[h] != 0.0f && kj < seq_len) {
-          float lg;
-          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg)
-              : "f"(p.g[static_cast<size_t>(seq_start + kj) * p.g_cols + h / p.g_group]));
+          const float lg = tg::log2_gate(p.g[static_cast<size_t>(seq_start + kj) * p.g_cols + h / p.g_group]);
           bias2 = p.beta[h] * lg;
         }
         ch = p.scale[h];
@@ -734,9 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = lane * 4 + u, kj = j * kTile + c;
         float v = 0.0f;  // keys past the sequence sit only in the diagonal tile, after every valid query
         if (p.g != nullptr && beta != 0.0f && kj < seq_len) {
-          float lg;
-          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg)
-              : "f"(p.g[static_cast<size_t>(seq_start + kj) * p.g_cols + gcol]));
+          const float lg = tg::log2_gate(p.g[static_cast<size_t>(seq_start + kj) * p.g_cols + gcol]);
           v = beta * lg;
         }
         dst[c] = v;

@@ -226,6 +226,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// Each lane of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // Each lane of the warp writes 32 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -258,6 +269,36 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16-byte global load through the read-only path without L1 allocation, and a streaming
+// 16-byte store (the row copies of the gather: each byte is touched once).
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_cs_v4(uint4 *p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Copy one row of n16 16-byte vectors with the 32 lanes of a warp, eight vectors per lane in
+// flight at a time.
+__device__ __forceinline__ void warp_copy_row(uint4 *dst, const uint4 *src, int n16, int lane) {
+  int v = lane;
+  for (; v + 32 * 7 < n16; v += 32 * 8) {
+    uint4 r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r[u] = ld_nc_v4(src + v + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) st_cs_v4(dst + v + 32 * u, r[u]);
+  }
+  for (; v < n16; v += 32) st_cs_v4(dst + v, ld_nc_v4(src + v));
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA / tensor core).
@@ -302,6 +343,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
 // ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
+
+// log2 of a gate value g >= 0, subnormal g included. The hardware log2 is taken on a normal
+// number only: a subnormal g (below 2^-126, a gate score under about -87.3) is first scaled by
+// 2^24, which is exact and makes it normal, and 24 is subtracted from the result
+// (log2(g 2^24) = log2(g) + 24). g = 0 gives -inf.
+__device__ __forceinline__ float log2_gate(float g) {
+  const bool sub = g < 1.17549435e-38f;  // the smallest normal fp32, 2^-126
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(sub ? g * 16777216.0f : g));
+  return sub ? y - 24.0f : y;
+}
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);

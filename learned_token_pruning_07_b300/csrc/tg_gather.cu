@@ -30,20 +30,6 @@ struct GatherParams {
   int32_t *status;
 };
 
-__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ void st_cs_v4(uint4 *p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
   tg::pdl_wait();
   tg::pdl_launch_dependents();
@@ -63,17 +49,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
       if (lane == 0) tg::report(p.status, TG_DEV_BAD_INDEX);
       continue;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.h + static_cast<size_t>(j) * p.d);
-    uint4 *dst = reinterpret_cast<uint4 *>(p.h_kept + static_cast<size_t>(m) * p.d);
-    int v = lane;
-    for (; v + 32 * 7 < nvec; v += 32 * 8) {
-      uint4 r[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) r[u] = ld_nc_v4(src + v + 32 * u);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) st_cs_v4(dst + v + 32 * u, r[u]);
-    }
-    for (; v < nvec; v += 32) st_cs_v4(dst + v, ld_nc_v4(src + v));
+    tg::warp_copy_row(reinterpret_cast<uint4 *>(p.h_kept + static_cast<size_t>(m) * p.d),
+                      reinterpret_cast<const uint4 *>(p.h + static_cast<size_t>(j) * p.d), nvec, lane);
     if (lane == 0) {
       if (p.pos_kept) {
         int pv;

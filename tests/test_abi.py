@@ -237,7 +237,7 @@ def _ctype_of(c_type):
     if c_type.endswith("*") or c_type == "tg_stream_t":
         return ctypes.c_void_p
     return {"int32_t": ctypes.c_int32, "tg_status": ctypes.c_int32, "float": ctypes.c_float,
-            "uint64_t": ctypes.c_uint64}[c_type]
+            "uint64_t": ctypes.c_uint64, "size_t": ctypes.c_size_t}[c_type]
 
 
 def test_binding_argument_types_match_the_header():
@@ -247,3 +247,32 @@ def test_binding_argument_types_match_the_header():
     for name, c_params in decls.items():
         _, argtypes = binding.SIGNATURES[name]
         assert [_ctype_of(t) for t in c_params] == list(argtypes), name
+
+
+def test_attention_workspace_size_by_hand(lib):
+    # Without a device the library plans for 148 SMs. Kept length 1,280 (the 32K sweep at K = 1024),
+    # 16 query / 8 kv heads of 128: 10 query tiles x 8 head pairs = 80 CTAs, fewer than 148, so the
+    # key ranges split. Chunks of c key tiles give sum_t ceil((t+1)/c) CTAs per head pair; at most
+    # 3 chunks per tile means c >= 4, and c = 4 gives 18 x 8 = 144 <= 148 CTAs.
+    # Bytes: 10 x 8 int32 counters rounded up to 256, then 8 x 18 slots of
+    # (2 x 128 x 128 + 2 x 128 x 2) fp32.
+    f = lib.tg_gated_attention_workspace_size
+    slot = (2 * 128 * 128 + 2 * 128 * 2) * 4
+    if os.environ.get("CUDA_VISIBLE_DEVICES", "") == "" and not _has_gpu():
+        assert f(1, 1280, 16, 8, 128) == 512 + 8 * 18 * slot
+    # K = 256: 4 query tiles. The heaviest tile walks only 4 key tiles, fewer than the 6 for which
+    # a split pays for its combine, so no split and no workspace.
+    assert f(1, 512, 16, 8, 128) == 0
+    # 34 query tiles x 8 pairs = 272 CTAs already fill the machine: no split, no workspace
+    assert f(1, 4352, 16, 8, 128) == 0
+    assert f(1, 100, 16, 8, 128) == 0          # one query tile: nothing to split
+    assert f(1, 1280, 16, 6, 128) == 0         # 16 % 6 != 0: invalid shape
+    assert f(0, 1280, 16, 8, 128) == 0
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False

@@ -79,6 +79,25 @@ def test_attention_strong_gates_and_zero_gates():
     assert np.all(ref == 0.0) and np.all(got == 0.0)
 
 
+def test_attention_subnormal_gates_keep_their_weight():
+    # Gates below the smallest normal fp32 (2^-126 ~ 1.18e-38; a score under about -87.3) are
+    # still gates: each key keeps the weight g^beta. With every key subnormal, a kernel that
+    # flushed them to zero would output zero rows; the oracle gives proper weighted averages.
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    M = 300
+    rng = np.random.default_rng(17)
+    g = (rng.uniform(1.0, 50.0, M) * 1e-40).astype(np.float32)
+    assert np.all(g < np.finfo(np.float32).tiny) and np.all(g > 0)
+    got, ref = _run(wl, [M], g_override=g)
+    assert np.all(np.abs(ref).max(axis=(1, 2)) > 0.0)
+    _assert_close(got, ref)
+    # a mix: subnormal keys beside normal ones, over several key tiles
+    M2 = 700
+    g2 = rng.uniform(0.05, 1.0, M2).astype(np.float32)
+    g2[: M2 // 2] = (rng.uniform(1.0, 50.0, M2 // 2) * 1e-41).astype(np.float32)
+    _assert_close(*_run(wl, [M2], g_override=g2, tag=5))
+
+
 def test_attention_odd_group_one_head_per_cta():
     wl = I.with_changes(I.WORKLOADS["qwen3_1p7b_8k"], H_q=6, H_kv=2)   # group of 3
     _assert_close(*_run(wl, [333]))
@@ -152,3 +171,89 @@ def test_attention_long_context_full_causal_sampled_rows():
     ref = O.gated_attention(Q64, I.bf16_bits_to_f64(at["K"]), I.bf16_bits_to_f64(at["V"]), None, cu,
                             at["tau"].astype(np.float64), beta.astype(np.float64), rows=rows)
     _assert_close(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# Split key ranges (tg_gated_attention_ws): short kept sequences, where one CTA per query tile
+# would leave SMs idle, against the oracle and against the unsplit kernel
+# ---------------------------------------------------------------------------
+
+def _run_ws(wl, lens, tag=0, repeats=2):
+    cu = I.cu_seqlens_of(lens)
+    M = int(cu[-1])
+    at = I.make_attention_inputs(wl, M, tag_extra=tag)
+    Qd, Kd, Vd, gd, cud = dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(at["g"]), dev(cu)
+    mx = max(lens)
+    ws = tg.attention_workspace(len(lens), mx, wl.H_q, wl.H_kv, wl.d_h)
+    outs = []
+    for _ in range(repeats):
+        O_d = torch.full((M, wl.H_q, wl.d_h), 0x7FC0, dtype=torch.int16, device="cuda")
+        st = status_word()
+        tg.gated_attention(Qd, Kd, Vd, cud, at["tau"], at["beta"], O_d, max_seqlen=mx, g=gd, status=st,
+                           workspace=ws)
+        torch.cuda.synchronize()
+        assert int(host(st)[0]) == 0
+        outs.append(host(O_d))
+    plain = torch.full((M, wl.H_q, wl.d_h), 0x7FC0, dtype=torch.int16, device="cuda")
+    tg.gated_attention(Qd, Kd, Vd, cud, at["tau"], at["beta"], plain, max_seqlen=mx, g=gd)
+    torch.cuda.synchronize()
+    ref = O.gated_attention(I.bf16_bits_to_f64(at["Q"]), I.bf16_bits_to_f64(at["K"]), I.bf16_bits_to_f64(at["V"]),
+                            at["g"].astype(np.float64), cu, at["tau"].astype(np.float64),
+                            at["beta"].astype(np.float64))
+    return ws, outs, host(plain), ref
+
+
+@pytest.mark.parametrize("wname,M", [("sweep_32k", 1024 + 256), ("qwen3_1p7b_8k", 1024 + 128)])
+def test_split_attention_at_the_small_budgets(wname, M):
+    # K = 1024 kept from the 32K sweep (1,280 rows) and from the 8K gate layer (1,152 rows):
+    # 10 and 9 query tiles x 8 head pairs leave SMs idle, so the key ranges split
+    wl = I.WORKLOADS[wname]
+    ws, outs, plain, ref = _run_ws(wl, [M], tag=M)
+    assert ws.numel() > 0                                   # this shape splits
+    got = I.bf16_bits_to_f64(outs[0])
+    _assert_close(got, ref)
+    assert np.array_equal(outs[0], outs[1])                 # chunks combine in a fixed order
+    # against the unsplit kernel: both within bf16 rounding of the same values
+    assert np.max(np.abs(got - I.bf16_bits_to_f64(plain))) <= 2 * ATTN_MAX_ABS
+    n_cnt = ws.view(torch.int32)[:64].cpu().numpy()
+    assert np.all(n_cnt == 0)                               # arrival counters are left at zero
+
+
+def test_split_attention_ragged_and_empty_tail_tiles():
+    # two sequences of different length: the shorter one has no query tiles past its end
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    ws, outs, plain, ref = _run_ws(wl, [900, 300], tag=21)
+    assert ws.numel() > 0
+    _assert_close(I.bf16_bits_to_f64(outs[0]), ref)
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_split_attention_dh64():
+    wl = I.WORKLOADS["tiny"]
+    ws, outs, plain, ref = _run_ws(wl, [1000], tag=22)
+    assert ws.numel() > 0
+    _assert_close(I.bf16_bits_to_f64(outs[0]), ref)
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("M", [4096 + 256, 256 + 256])
+def test_workspace_call_without_split_is_the_plain_kernel(M):
+    # enough query tiles for every SM (K = 4096), or too few key tiles for a split to pay (K = 256):
+    # no workspace needed, and the result is bit-identical to the plain call
+    wl = I.WORKLOADS["sweep_32k"]
+    assert tg.gated_attention_workspace_size(1, M, wl.H_q, wl.H_kv, wl.d_h) == 0
+    ws, outs, plain, ref = _run_ws(wl, [M], tag=23, repeats=1)
+    assert np.array_equal(outs[0], plain)
+
+
+def test_split_attention_rejects_a_small_workspace():
+    wl = I.WORKLOADS["sweep_32k"]
+    M = 1024 + 256
+    n = tg.gated_attention_workspace_size(1, M, wl.H_q, wl.H_kv, wl.d_h)
+    at = I.make_attention_inputs(wl, M)
+    small = torch.zeros(n - 256, dtype=torch.uint8, device="cuda")
+    O_d = torch.zeros((M, wl.H_q, wl.d_h), dtype=torch.int16, device="cuda")
+    with pytest.raises(tg.TGError) as e:
+        tg.gated_attention(dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(I.cu_seqlens_of([M])), at["tau"],
+                           at["beta"], O_d, max_seqlen=M, g=dev(at["g"]), workspace=small)
+    assert e.value.status == tg.TG_ERR_INVALID_ARG

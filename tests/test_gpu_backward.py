@@ -25,10 +25,12 @@ from tests._helpers import bf16_dev_to_f64, dev, host, status_word
 pytestmark = pytest.mark.gpu
 
 
-def _case(wl, lens, seed, use_g=True, beta_zero=False):
+def _case(wl, lens, seed, use_g=True, beta_zero=False, g_override=None):
     cu = I.cu_seqlens_of(lens)
     M = int(cu[-1])
     at = I.make_attention_inputs(wl, M, tag_extra=seed)
+    if g_override is not None:
+        at["g"] = g_override
     rng = np.random.default_rng(300 + seed)
     dO = I.f32_to_bf16_bits(rng.standard_normal((M, wl.H_q, wl.d_h)).astype(np.float32))
     tau, beta = at["tau"], np.zeros_like(at["beta"]) if beta_zero else at["beta"]
@@ -163,6 +165,16 @@ def test_backward_without_gate_and_with_beta_zero():
     wl = I.WORKLOADS["qwen3_1p7b_8k"]
     _case(wl, [150], seed=7, use_g=False)
     _case(wl, [150], seed=8, beta_zero=True)
+
+
+def test_backward_with_subnormal_gates():
+    # every key's gate below the smallest normal fp32: the key bias is beta_h ln g_j of the
+    # subnormal value itself (no flush to zero), in the forward and in both backward passes
+    wl = I.WORKLOADS["qwen3_1p7b_8k"]
+    M = 200
+    g = (np.random.default_rng(41).uniform(1.0, 50.0, M) * 1e-40).astype(np.float32)
+    assert np.all(g < np.finfo(np.float32).tiny) and np.all(g > 0)
+    _case(wl, [M], seed=12, g_override=g)
 
 
 def test_gate_score_gradient_through_kept_rows():
