@@ -36,6 +36,23 @@ import numpy as np  # noqa: E402
 METRIC = "gated-prefill tokens/s (score+topK+gather+gated attn), N=32K; % of roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed between timed steps, outside the per-step events: a 256 MB write, then a 256 MB read of a "
+           "second buffer, so the step's inputs start in HBM and L2 holds no dirty lines for the first kernel")
+
+
+class L2Flush:
+    """Evicts the step's inputs from the 126 MB L2 between timed steps: a write of one buffer larger
+    than L2, then a read of a second one, which also writes back the first buffer's dirty lines
+    before the next step starts (otherwise the first kernel of the step pays for that write-back)."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink.copy_(self.r.sum().reshape(1))
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
 
@@ -220,10 +237,16 @@ class GatedPrefill:
         self.w2 = dev(pinned(gi["w2"]))
         e = lambda *shape, dt=torch.float32: torch.empty(*shape, dtype=dt, device="cuda")
         self.s, self.g = e(T), e(T)
+        # the tie-heavy workload selects from its synthetic 256-level score buffer; the others rank
+        # the scores the step itself computes
+        self.s_sel = self.s if not wl.score_levels else torch.from_numpy(I.make_scores(wl)).cuda()
         self.kept, self.cu_kept = e(T, dt=torch.int32), e(B + 1, dt=torch.int32)
         self.h_kept = e(T, wl.d, dt=torch.int16)
         self.pos_kept, self.g_kept = e(T, dt=torch.int32), e(T)
         self.O = e(self.M, wl.H_q, wl.d_h, dt=torch.int16)
+        # attention workspace: used when one CTA per query tile would leave SMs idle (short kept
+        # sequences); empty otherwise. Zero-filled once; each call leaves it zeroed.
+        self.ws = tg.attention_workspace(B, self.max_seqlen, wl.H_q, wl.H_kv, wl.d_h)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.O_host = torch.empty(self.O.shape, dtype=torch.int16).pin_memory()
         self.cu_kept_host = torch.empty(B + 1, dtype=torch.int32).pin_memory()
@@ -236,13 +259,14 @@ class GatedPrefill:
         rec(ev[0])
         tg.gate_score(d["h"], self.W1, self.w2, self.s, self.g, instr_mask=d["mask"], status=self.status)
         rec(ev[1])
-        tg.topk_select(self.s, d["cu"], self.K, self.kept, self.cu_kept, instr_mask=d["mask"], status=self.status)
+        tg.topk_select(self.s_sel, d["cu"], self.K, self.kept, self.cu_kept, instr_mask=d["mask"],
+                       status=self.status)
         rec(ev[2])
         tg.gather_kept(d["h"], d["cu"], self.kept, self.cu_kept, self.h_kept, pos=d["pos"], g=self.g,
                        pos_kept=self.pos_kept, g_kept=self.g_kept, status=self.status)
         rec(ev[3])
         tg.gated_attention(d["Q"], d["K"], d["V"], self.cu_kept, self.tau, self.beta, self.O,
-                           max_seqlen=self.max_seqlen, g=self.g_kept, status=self.status)
+                           max_seqlen=self.max_seqlen, g=self.g_kept, status=self.status, workspace=self.ws)
         rec(ev[4])
 
     def step_e2e(self):
@@ -255,7 +279,7 @@ class GatedPrefill:
                             self.h_kept, pos_kept=self.pos_kept, g_kept=self.g_kept, pos=d["pos"],
                             instr_mask=d["mask"], status=self.status)
         tg.gated_attention(d["Q"], d["K"], d["V"], self.cu_kept, self.tau, self.beta, self.O,
-                           max_seqlen=self.max_seqlen, g=self.g_kept, status=self.status)
+                           max_seqlen=self.max_seqlen, g=self.g_kept, status=self.status, workspace=self.ws)
         self.O_host.copy_(self.O, non_blocking=True)
         self.cu_kept_host.copy_(self.cu_kept, non_blocking=True)
 
@@ -310,9 +334,9 @@ class GraphStep:
 def warm(gstep, warmup, torch, flush):
     for _ in range(warmup):
         gstep.replay()
-        flush.zero_()
+        flush()
         gstep.replay(staged=True)
-        flush.zero_()
+        flush()
     torch.cuda.synchronize()
 
 
@@ -321,7 +345,7 @@ def time_whole_steps(gstep, steps, torch, flush):
     events) and each step's time is read before the next."""
     per_step = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         gstep.replay()
         torch.cuda.synchronize()
         per_step.append(gstep.step_time())
@@ -332,7 +356,7 @@ def time_stages(gstep, steps, torch, flush):
     """The per-kernel breakdown: replays of the staged graph, L2 flushed between steps."""
     per_stage = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         gstep.replay(staged=True)
         torch.cuda.synchronize()
         per_stage.append(gstep.times())
@@ -367,68 +391,111 @@ def blas_threads():
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
+        return max(n) if n else (os.cpu_count() or 1)
     except Exception:
         return os.cpu_count() or 1
 
 
-def oracle_sample_step(wl, K, frac, cache):
-    """Time the oracle on a bounded sample of one step and scale to the full step.
-
-    Sample: the score MLP on every 1/frac-th row; selection and gather on the whole batch
-    (their input scores are the seeded synthetic buffer); attention on every 1/frac-th query
-    row. Scores and attention are scaled by their share of the full work. Returns
-    (estimated full-step seconds, seconds actually spent)."""
+def _oracle_inputs(wl, K, cache):
+    """The step's seeded inputs, widened once for the oracle (not timed)."""
     from learned_token_pruning_07_b300 import inputs as I
-    from oracle import tokengate_oracle as O
     if "gi" not in cache:
         gi = I.make_gate_inputs(wl)
         cache["gi"] = gi
         cache["h64"] = I.bf16_bits_to_f64(gi["h"])
         cache["W1"] = I.bf16_bits_to_f64(gi["W1"])
         cache["w2"] = I.bf16_bits_to_f64(gi["w2"])
-        cache["s"] = I.make_scores(wl)
         kept_lens = [min(K, a) + b for a, b in zip(wl.doc_lens, wl.instr_lens)]
         at = I.make_attention_inputs(wl, sum(kept_lens))
         cache["at"] = {k: (I.bf16_bits_to_f64(v) if k in ("Q", "K", "V") else v) for k, v in at.items()}
-        cache["cu_k"] = I.cu_seqlens_of(kept_lens)
-    gi, at = cache["gi"], cache["at"]
-    rows = np.arange(0, wl.T_total, frac)
+        # a workload whose selection scores are quantised (the tie-heavy ragged batch) selects
+        # from its synthetic quantised buffer, as the GPU step does
+        cache["s_sel"] = I.make_scores(wl) if wl.score_levels else None
+    return cache
+
+
+def oracle_step(wl, K, cache):
+    """One whole, unsampled step of the oracle on the step's inputs: score every row, select,
+    gather, then gated attention over every kept row. Returns the seconds of each stage."""
+    from oracle import tokengate_oracle as O
+    c = _oracle_inputs(wl, K, cache)
+    gi, at = c["gi"], c["at"]
     t0 = time.perf_counter()
-    O.gate_score(cache["h64"][rows], cache["W1"], cache["w2"], gi["instr_mask"][rows])
+    s, g = O.gate_score(c["h64"], c["W1"], c["w2"], gi["instr_mask"])
     t1 = time.perf_counter()
-    kept, cu_kept = O.topk_select(cache["s"], gi["instr_mask"], gi["cu_seqlens"], K)
-    O.gather_kept(gi["h"], gi["pos"], cache["s"], kept, gi["cu_seqlens"])
+    s_sel = c["s_sel"] if c["s_sel"] is not None else s.astype(np.float32)
+    kept, cu_kept = O.topk_select(s_sel, gi["instr_mask"], gi["cu_seqlens"], K)
     t2 = time.perf_counter()
-    cu_k = cache["cu_k"]
-    M = int(cu_k[-1])
-    qrows = np.arange(0, M, frac)
-    O.gated_attention(at["Q"], at["K"], at["V"], at["g"].astype(np.float64), cu_k,
-                      at["tau"].astype(np.float64), at["beta"].astype(np.float64), rows=qrows)
+    _, _, g_kept = O.gather_kept(gi["h"], gi["pos"], g, kept, gi["cu_seqlens"])
     t3 = time.perf_counter()
-    seq_of = np.searchsorted(cu_k, qrows, side="right") - 1
-    sampled_pairs = float(np.sum(qrows - cu_k[seq_of] + 1))
-    lens = np.diff(cu_k)
-    full_pairs = float(np.sum(lens * (lens + 1) / 2))
-    est = (t1 - t0) * (wl.T_total / len(rows)) + (t2 - t1) + (t3 - t2) * (full_pairs / max(sampled_pairs, 1.0))
-    return est, t3 - t0
+    O.gated_attention(at["Q"], at["K"], at["V"], g_kept, cu_kept, at["tau"].astype(np.float64),
+                      at["beta"].astype(np.float64))
+    t4 = time.perf_counter()
+    return {"score": t1 - t0, "select": t2 - t1, "gather": t3 - t2, "attention": t4 - t3, "step": t4 - t0}
 
 
-def cpu_baseline(wl, K, frac, min_s=10.0, budget_s=30.0):
-    """The oracle as it stands, on repeated bounded samples of one step: at least min_s seconds
-    of CPU work and at least three samples, stopping once budget_s is spent; the median
-    estimate of the full step gives the value."""
+_ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                   "NUMEXPR_NUM_THREADS")
+
+
+def oracle_stage_threads(wl, K, cache):
+    """Score, select and gather of the oracle on every BLAS thread (this process) and on one
+    thread (a child process started with the BLAS thread counts set to 1)."""
+    all_cores = {k: v * 1000.0 for k, v in oracle_step_front(wl, K, cache).items()}
+    env = dict(os.environ)
+    env.update({k: "1" for k in _ONE_THREAD_ENV})
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from learned_token_pruning_07_b300 import inputs as I; "
+            "t = bench.oracle_step_front(I.WORKLOADS[%r], %d, {}); print(json.dumps(t))") % (ROOT, wl.name, K)
+    single = None
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        if r.returncode == 0:
+            single = {k: v * 1000.0 for k, v in json.loads(r.stdout.strip().splitlines()[-1]).items()}
+    except (OSError, subprocess.TimeoutExpired, ValueError, IndexError):
+        single = None
+    return {"all_cores": all_cores, "single_thread": single, "unit": "ms",
+            "threads_all_cores": blas_threads()}
+
+
+def oracle_step_front(wl, K, cache):
+    """The oracle's score, select and gather of one step (attention left out), in seconds."""
+    from oracle import tokengate_oracle as O
+    c = _oracle_inputs(wl, K, cache)
+    gi = c["gi"]
+    t0 = time.perf_counter()
+    s, g = O.gate_score(c["h64"], c["W1"], c["w2"], gi["instr_mask"])
+    t1 = time.perf_counter()
+    s_sel = c["s_sel"] if c["s_sel"] is not None else s.astype(np.float32)
+    kept, _ = O.topk_select(s_sel, gi["instr_mask"], gi["cu_seqlens"], K)
+    t2 = time.perf_counter()
+    O.gather_kept(gi["h"], gi["pos"], g, kept, gi["cu_seqlens"])
+    t3 = time.perf_counter()
+    return {"score": t1 - t0, "select": t2 - t1, "gather": t3 - t2}
+
+
+def oracle_sample_text(n_steps, spent):
+    return (f"{n_steps} whole unsampled oracle step(s) of this workload (numpy fp64: every row scored, full "
+            f"select and gather, attention over every kept row), {spent:.1f} s of CPU time; value = tokens / "
+            f"median step time")
+
+
+def cpu_baseline(wl, K, min_s=10.0, max_steps=3):
+    """The oracle as it stands, timed on whole steps of the same workload (at least one, until
+    min_s seconds are spent, at most max_steps), plus the single-thread and all-core times of
+    its score, select and gather stages. The same measurement as the reference arm's steps."""
     cache = {}
-    ests, spent = [], 0.0
-    while (spent < min_s or len(ests) < 3) and spent < budget_s:
-        e, s = oracle_sample_step(wl, K, frac, cache)
-        ests.append(e)
-        spent += s
-    est = statistics.median(ests)
-    return {"value": wl.T_total / est, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"numpy fp64 oracle: score MLP on every {frac}th row, full select+gather, "
-                       f"attention on every {frac}th query row; scaled by work share "
-                       f"({len(ests)} reps, {spent:.1f} s)")}
+    steps, spent = [], 0.0
+    while (spent < min_s and len(steps) < max_steps) or not steps:
+        t = oracle_step(wl, K, cache)
+        steps.append(t)
+        spent += t["step"]
+    med = statistics.median([t["step"] for t in steps])
+    stage_ms = {k: 1000.0 * statistics.median([t[k] for t in steps]) for k in steps[0]}
+    return {"value": wl.T_total / med, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "ms_per_step": 1000.0 * med, "stage_ms": stage_ms,
+            "front_stages_by_threads": oracle_stage_threads(wl, K, cache),
+            "sample": oracle_sample_text(len(steps), spent)}
 
 
 # ---------------------------------------------------------------------------
@@ -463,7 +530,7 @@ def long_context(torch, flush, steps):
     torch.cuda.synchronize()
     times = []
     for _ in range(3):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         call()
@@ -478,7 +545,7 @@ def long_context(torch, flush, steps):
     pruned_attn_ms = float(pst[:, 3].mean())
     return {"workload": workload_label(wl, wl.K) + "; full causal attention over all tokens",
             "pruned_step_ms": float(ps.mean()), "pruned_tokens_per_s": wl.T_total / (float(ps.mean()) / 1000.0),
-            "pruned_stage_us": [float(x) * 1000.0 for x in pst.mean(axis=0)],
+            "pruned_stage_us": [float(x) * 1000.0 for x in pst.mean(axis=0)], "stage_names": STAGE_NAMES,
             "pruned_attention_tflops": wk["gated_attention"]["flops"] / (pruned_attn_ms * 1e-3) / 1e12,
             "full_attention_ms": full_ms, "full_attention_tflops": full_flops / (full_ms * 1e-3) / 1e12,
             "attention_time_ratio_full_over_pruned": full_ms / pruned_attn_ms}
@@ -507,7 +574,7 @@ def paper_form(path, torch, flush, steps):
         torch.cuda.synchronize()
         ts = []
         for _ in range(max(3, min(steps, 20))):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -571,7 +638,7 @@ def two_budget(path, torch, flush, steps):
         torch.cuda.synchronize()
         ts = []
         for _ in range(max(3, min(steps, 10))):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -622,7 +689,7 @@ def backward(path, torch, flush, steps):
         torch.cuda.synchronize()
         ts = []
         for _ in range(max(3, min(steps, 10))):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -676,7 +743,7 @@ def heads(path, torch, flush, steps):
         torch.cuda.synchronize()
         ts = []
         for _ in range(max(3, min(steps, 20))):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -693,6 +760,74 @@ def heads(path, torch, flush, steps):
     return out
 
 
+STAGE_NAMES = ["gate_score", "topk_select", "gather_kept", "gated_attention"]
+
+
+def stage_summary(work, per_stage, peaks):
+    """Per-kernel mean time and roofline fraction from the staged graph's event times (ms)."""
+    stages = {}
+    for i, n in enumerate(STAGE_NAMES):
+        us = float(per_stage[:, i].mean()) * 1000.0
+        w = work[n]
+        if w["bound"] == "tensor":
+            ach = w["flops"] / (us * 1e-6) / 1e12
+            stages[n] = {"us": us, "bound": "tensor", "achieved_tflops": ach, "frac": ach / peaks["bf16_tflops"],
+                         "achieved_gbs": w["bytes"] / (us * 1e-6) / 1e9}
+        else:
+            ach = w["bytes"] / (us * 1e-6) / 1e9
+            stages[n] = {"us": us, "bound": "hbm", "achieved_gbs": ach, "frac": ach / peaks["hbm_gbs"]}
+    return stages
+
+
+def select_gather_summary(work, stages, peaks):
+    """Selection and gather together against HBM: selection alone moves too few bytes to mean
+    anything against HBM bandwidth."""
+    us = stages["topk_select"]["us"] + stages["gather_kept"]["us"]
+    by = work["topk_select"]["bytes"] + work["gather_kept"]["bytes"]
+    return {"us": us, "bytes": by, "achieved_gbs": by / (us * 1e-6) / 1e9,
+            "frac": by / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+
+
+def other_configs(torch, flush, steps, peaks, rank):
+    """Throughput lines of the other single-GPU workloads: the Qwen3-1.7B-shaped 8K gate layer
+    (K = 1024) and the ragged batch of eight sequences (K = 2048 each, selection on 256-level
+    scores), each with its per-kernel times and roofline fractions."""
+    from learned_token_pruning_07_b300 import inputs as I
+    out = []
+    for name in ("qwen3_1p7b_8k", "ragged_b8"):
+        base = I.WORKLOADS[name]
+        wl = I.with_changes(base, seed=replica_seed(base.seed, rank))
+        p = GatedPrefill(wl, wl.K, torch)
+        g = GraphStep(p, torch)
+        warm(g, 3, torch, flush)
+        ps, pst = time_device_steps(g, max(5, min(steps, 30)), torch, flush)
+        assert p.tg.read_device_status(p.status) == 0, "device reported an error"
+        work = stage_work(wl, wl.K, p.kept_lens)
+        st = stage_summary(work, pst, peaks)
+        ms = float(ps.mean())
+        out.append({"workload": workload_label(base, wl.K), "K": wl.K, "T_total": wl.T_total, "M_kept": p.M,
+                    "value": wl.T_total / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "stages": st,
+                    "select_plus_gather": select_gather_summary(work, st, peaks),
+                    "selection_scores": ("synthetic 256-level quantised buffer" if wl.score_levels
+                                         else "the step's own gate scores")})
+        del g, p
+        torch.cuda.empty_cache()
+    return out
+
+
+TIMING_NOTE = ("step captured in a CUDA graph (events only around the step, kernels chained by programmatic "
+               "dependent launch); per-kernel times from a second graph with events between the kernels, on the "
+               "launching stream; mean over steps; max over ranks")
+
+
+def config_dict(wl, K, world):
+    """The workload's description, the same in the GPU line and in the reference arm's line."""
+    M = sum(min(K, a) + b for a, b in zip(wl.doc_lens, wl.instr_lens))
+    return {"workload": workload_label(wl, K), "K": K, "T_total": wl.T_total, "M_kept": M,
+            "parallelism": f"replicas x{world} (independent batches, no collective)", "l2": L2_NOTE,
+            "timing": TIMING_NOTE}
+
+
 def workload_label(wl, K):
     docs = wl.doc_lens if wl.B > 1 else wl.doc_lens[0]
     ins = wl.instr_lens if wl.B > 1 else wl.instr_lens[0]
@@ -701,30 +836,27 @@ def workload_label(wl, K):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle, timed on whole unsampled steps of the same workload on the
+    host cores (rank 0 only; other ranks exit without work)."""
     from learned_token_pruning_07_b300 import inputs as I
     if rank != 0:
         return 0
     wl = I.WORKLOADS[args.workload]
     K = args.k if args.k is not None else wl.K
     cache = {}
-    frac = args.oracle_frac
     for _ in range(args.warmup):
-        oracle_sample_step(wl, K, frac, cache)
-    ests, spent = [], 0.0
-    for _ in range(args.steps):
-        e, s = oracle_sample_step(wl, K, frac, cache)
-        ests.append(e)
-        spent += s
-    ms = 1000.0 * float(np.mean(ests))
+        oracle_step(wl, K, cache)
+    steps = [oracle_step(wl, K, cache) for _ in range(args.steps)]
+    spent = sum(t["step"] for t in steps)
+    ms = 1000.0 * spent / len(steps)
     value = wl.T_total / (ms / 1000.0)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_label(wl, K), "K": K, "T_total": wl.T_total},
+            "config": config_dict(wl, K, world),
+            "stage_ms": {k: 1000.0 * sum(t[k] for t in steps) / len(steps) for k in steps[0]},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": (f"each step: score MLP on every {frac}th row, full select+gather, "
-                                        f"attention on every {frac}th query row, scaled by work share; "
-                                        f"{spent:.1f} s of CPU time in the timed steps")},
+                             "sample": oracle_sample_text(len(steps), spent)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -743,7 +875,7 @@ def run_gpu(args, rank, world, local):
     K = args.k if args.k is not None else base.K
     wl = I.with_changes(base, seed=replica_seed(base.seed, rank))
     path = GatedPrefill(wl, K, torch)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(torch)
     torch.cuda.synchronize()
 
     # correctness gate before timing: the device status word must stay clean
@@ -771,7 +903,7 @@ def run_gpu(args, rank, world, local):
     t_end = time.perf_counter() + max(0.0, 1.0 - wall)
     while time.perf_counter() < t_end:
         gstep.replay()
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     assert path.tg.read_device_status(path.status) == 0, "device reported an error"
@@ -785,18 +917,8 @@ def run_gpu(args, rank, world, local):
 
     peaks = load_peaks()
     work = stage_work(wl, K, path.kept_lens)
-    names = ["gate_score", "topk_select", "gather_kept", "gated_attention"]
-    stages = {}
-    for i, n in enumerate(names):
-        us = float(per_stage[:, i].mean()) * 1000.0
-        w = work[n]
-        if w["bound"] == "tensor":
-            ach = w["flops"] / (us * 1e-6) / 1e12
-            stages[n] = {"us": us, "bound": "tensor", "achieved_tflops": ach, "frac": ach / peaks["bf16_tflops"],
-                         "achieved_gbs": w["bytes"] / (us * 1e-6) / 1e9}
-        else:
-            ach = w["bytes"] / (us * 1e-6) / 1e9
-            stages[n] = {"us": us, "bound": "hbm", "achieved_gbs": ach, "frac": ach / peaks["hbm_gbs"]}
+    names = STAGE_NAMES
+    stages = stage_summary(work, per_stage, peaks)
     dom = max(names, key=lambda n: stages[n]["us"])
     w = work[dom]
     traffic = measured_traffic(dom, wl.name, K)
@@ -808,8 +930,6 @@ def run_gpu(args, rank, world, local):
         roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": stages[dom]["frac"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
-    sel_gather_us = stages["topk_select"]["us"] + stages["gather_kept"]["us"]
-    sg_bytes = work["topk_select"]["bytes"] + work["gather_kept"]["bytes"]
 
     sweep = []
     if args.sweep and base.budgets and rank == 0:
@@ -823,12 +943,13 @@ def run_gpu(args, rank, world, local):
             sweep.append({"K": Kb, "M_kept": p2.M, "ms_per_step": float(ps.mean()),
                           "value": wl.T_total / (float(ps.mean()) / 1000.0),
                           "attention_tflops": wk["gated_attention"]["flops"] / (a_us * 1e-6) / 1e12,
-                          "stage_us": [float(x) * 1000.0 for x in pst.mean(axis=0)]})
+                          "stage_us": [float(x) * 1000.0 for x in pst.mean(axis=0)], "stage_names": STAGE_NAMES})
             if p2 is not path:
                 del g2, p2
                 torch.cuda.empty_cache()
 
     extras = rank == 0 and args.extras
+    others = other_configs(torch, flush, args.steps, peaks, rank) if (rank == 0 and args.configs) else None
     paper = paper_form(path, torch, flush, args.steps) if extras else None
     twob = two_budget(path, torch, flush, args.steps) if extras else None
     bwd = backward(path, torch, flush, args.steps) if extras else None
@@ -837,23 +958,17 @@ def run_gpu(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(base, K, args.oracle_frac)
+        cpu = cpu_baseline(base, K)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_label(base, K), "K": K, "T_total": wl.T_total, "M_kept": path.M,
-                       "parallelism": f"replicas x{world} (independent batches, no collective)",
-                       "l2": "flushed between timed steps (256 MB write, outside the per-step events)",
-                       "timing": ("step captured in a CUDA graph (events only around the step, kernels chained "
-                                  "by programmatic dependent launch); per-kernel times from a second graph with "
-                                  "events between the kernels, on the launching stream; mean over steps; max over ranks")},
+            "config": config_dict(base, K, world),
             "roofline": roof,
             "stages": stages,
-            "select_plus_gather": {"us": sel_gather_us, "achieved_gbs": sg_bytes / (sel_gather_us * 1e-6) / 1e9,
-                                   "frac": sg_bytes / (sel_gather_us * 1e-6) / 1e9 / peaks["hbm_gbs"]},
+            "select_plus_gather": select_gather_summary(work, stages, peaks),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": path.h2d_bytes(), "d2h_bytes_per_step": path.d2h_bytes(),
@@ -864,6 +979,8 @@ def run_gpu(args, rank, world, local):
         }
         if sweep:
             line["sweep"] = sweep
+        if others:
+            line["configs"] = others
         if paper:
             line["paper_form"] = paper
         if twob:
@@ -892,9 +1009,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--long-context", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the 128K workload: pruned step vs full causal attention")
+    ap.add_argument("--configs", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the 8K gate layer and the ragged batch of eight sequences")
     ap.add_argument("--extras", action=argparse.BooleanOptionalAction, default=True,
                     help="also measure the paper form, the two-budget pack, the backward and per-head gates")
-    ap.add_argument("--oracle-frac", type=int, default=8)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

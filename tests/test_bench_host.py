@@ -105,3 +105,35 @@ def test_reference_arm_prints_only_on_rank_zero():
     out = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "tiny",
                      env_extra={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert out == []
+
+
+def test_cpu_baseline_times_whole_unsampled_oracle_steps():
+    # the tiny workload: every row scored, every kept row attended; stage times add up to the step
+    wl = I.WORKLOADS["tiny"]
+    cache = {}
+    t = bench.oracle_step(wl, wl.K, cache)
+    assert set(t) == {"score", "select", "gather", "attention", "step"}
+    parts = t["score"] + t["select"] + t["gather"] + t["attention"]
+    assert 0.0 < parts <= t["step"] * 1.0001 + 1e-6
+    cpu = bench.cpu_baseline(wl, wl.K, min_s=0.0, max_steps=1)
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1
+    assert cpu["value"] == pytest.approx(wl.T_total / (cpu["ms_per_step"] / 1000.0))
+    assert "unsampled" in cpu["sample"] and "1 whole" in cpu["sample"]
+    thr = cpu["front_stages_by_threads"]
+    assert thr["single_thread"] is not None and thr["threads_all_cores"] >= 1
+    assert set(thr["single_thread"]) == set(thr["all_cores"]) == {"score", "select", "gather"}
+
+
+def test_stage_summary_fractions_use_the_measured_peaks():
+    import numpy as np
+    wl = I.WORKLOADS["sweep_32k"]
+    work = bench.stage_work(wl, 4096, [4352])
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1500.0}
+    per_stage = np.array([[0.05, 0.01, 0.01, 0.1]])          # ms per stage
+    st = bench.stage_summary(work, per_stage, peaks)
+    assert st["gate_score"]["frac"] == pytest.approx(work["gate_score"]["flops"] / 50e-6 / 1e12 / 1500.0)
+    assert st["gather_kept"]["frac"] == pytest.approx(work["gather_kept"]["bytes"] / 10e-6 / 1e9 / 6000.0)
+    sg = bench.select_gather_summary(work, st, peaks)
+    assert sg["us"] == pytest.approx(20.0)
+    assert sg["frac"] == pytest.approx((work["topk_select"]["bytes"] + work["gather_kept"]["bytes"]) / 20e-6 / 1e9
+                                       / 6000.0)
