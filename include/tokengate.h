@@ -230,6 +230,29 @@ TG_API tg_status tg_gated_attention_ws(const uint16_t *Q, const uint16_t *K, con
                                 tg_stream_t stream);
 
 /*
+ * tg_gated_attention_noalloc — tg_gated_attention_ws without a caller workspace, for callers that
+ *   cannot allocate device memory: code running while another allocator owns the device's memory
+ *   (a framework's caching pool, a serving runtime that reserves all memory up front), or code
+ *   whose hot path must not allocate. It has no counterpart in the TokenGate pages: it only moves
+ *   the split launch's scratch from the caller into the library.
+ *   The scratch is a fixed 16 MiB array in device memory that every GPU loading this library
+ *   holds until the process exits; the call itself allocates and frees nothing. A shape whose
+ *   split needs more than 16 MiB (tg_gated_attention_workspace_size above it) returns
+ *   TG_ERR_UNSUPPORTED and launches nothing; use tg_gated_attention_ws for it.
+ *   The first call on a device looks up the array's device address; make that first call
+ *   before any stream capture on that device. Every call clears the array's arrival counters on
+ *   the stream before its kernel. All calls on a device share the one array: calls whose
+ *   kernels overlap on the GPU (other streams, other host threads) race on it and must not run
+ *   concurrently.
+ *   Arguments, layouts, results and other errors as tg_gated_attention.
+ */
+TG_API tg_status tg_gated_attention_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                            const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
+                                            int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                            int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                            int32_t *status, tg_stream_t stream);
+
+/*
  * tg_gated_attention_lse — tg_gated_attention that also writes, for every kept row i and query
  *   head h, lse[i * H_q + h] = ln sum_{j <= i} exp(tau_h q_i.k_j / sqrt(d_h) + beta_h ln g_j)
  *   (-inf when every key has zero weight): what the backward needs to rebuild P.

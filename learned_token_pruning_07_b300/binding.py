@@ -37,6 +37,7 @@ SIGNATURES = {
     "tg_gated_attention_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "tg_gated_attention_ws": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t,
                                    _P, _P]),
+    "tg_gated_attention_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tg_gated_attention_lse": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tg_gated_attention_bwd": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _P, _P]),
@@ -203,6 +204,21 @@ def gated_attention(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, sta
         name = "tg_gated_attention_ws"
     del tau_a, beta_a
     _check(name, st)
+
+
+def gated_attention_noalloc(Q, K, V, cu_kept, tau, beta, O, max_seqlen: int, g=None, status=None, stream=None):
+    """tg_gated_attention_noalloc: the split launch's scratch is the library's fixed array, so the
+    caller passes no workspace (for callers that cannot allocate device memory)."""
+    M, H_q, d_h = Q.shape
+    H_kv = K.shape[1]
+    B = cu_kept.numel() - 1
+    tau_a, tau_p = _host_f32(tau)
+    beta_a, beta_p = _host_f32(beta)
+    st = load().tg_gated_attention_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(g), _heads(g), _ptr(cu_kept), B, M,
+                                           int(max_seqlen), H_q, H_kv, d_h, tau_p, beta_p, _ptr(O), _ptr(status),
+                                           _stream(stream))
+    del tau_a, beta_a
+    _check("tg_gated_attention_noalloc", st)
 
 
 def gated_attention_workspace_size(B: int, max_seqlen: int, H_q: int, H_kv: int, d_h: int) -> int:

@@ -31,6 +31,11 @@ tg_status launch_gated_attention(const uint16_t *Q, const uint16_t *K, const uin
                                  int32_t *status, cudaStream_t stream, float *lse = nullptr,
                                  void *workspace = nullptr, size_t workspace_bytes = 0);
 size_t gated_attention_workspace_size(int32_t B, int32_t max_seqlen, int32_t H_q, int32_t H_kv, int32_t d_h);
+tg_status launch_gated_attention_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                         const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
+                                         int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                         int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                         int32_t *status, cudaStream_t stream);
 tg_status launch_gated_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                                      const float *g, int32_t H_g, const uint16_t *O, const uint16_t *dO,
                                      const float *lse, const int32_t *cu_kept, int32_t B, int32_t M_cap,
@@ -205,6 +210,18 @@ tg_status tg_gated_attention_ws(const uint16_t *Q, const uint16_t *K, const uint
   return tg_host::launch_gated_attention(Q, K, V, g, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv,
                                          d_h, tau, beta, O, status, S(stream), nullptr, workspace,
                                          workspace_bytes);
+}
+
+tg_status tg_gated_attention_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                     const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
+                                     int32_t M_capacity, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                     int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                     int32_t *status, tg_stream_t stream) {
+  const tg_status st =
+      check_attention(Q, K, V, H_g, cu_kept, B, M_capacity, max_seqlen, H_q, H_kv, d_h, tau, beta, O);
+  if (st != TG_OK) return st;
+  return tg_host::launch_gated_attention_noalloc(Q, K, V, g, H_g, cu_kept, B, M_capacity, max_seqlen, H_q,
+                                                 H_kv, d_h, tau, beta, O, status, S(stream));
 }
 
 tg_status tg_gated_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V,

@@ -26,6 +26,7 @@
 // softmax runs on packed fp32 pairs (fma/add .f32x2) with 3-input max, and only the diagonal
 // key tile carries the causal mask.
 #include <algorithm>
+#include <mutex>
 
 #include "tg_common.cuh"
 
@@ -782,6 +783,12 @@ tg_status launch_attention_d(const uint16_t *Q, const uint16_t *K, const uint16_
 
 }  // namespace
 
+// The split workspace of tg_gated_attention_noalloc: a fixed 16 MiB array in device memory, which
+// every GPU that loads this library holds until the process exits. Host code only names it to
+// look up its device address (cudaGetSymbolAddress); the kernels receive that address.
+constexpr size_t kFixedScratchBytes = static_cast<size_t>(16) << 20;
+static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
+
 namespace tg_host {
 
 namespace {
@@ -921,6 +928,59 @@ tg_status launch_gated_attention_eq8(const uint16_t *Q, const uint16_t *K, const
   if (d_h == 128) return launch_attention_d<128, kEq8>(Q, K, V, p, stream);
   if (d_h == 64) return launch_attention_d<64, kEq8>(Q, K, V, p, stream);
   return TG_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// Attention for callers that cannot allocate device memory (tg_gated_attention_noalloc): the
+// split launch's workspace is a fixed array that the library itself holds on the device, so
+// such a caller never needs to hand one in. Its address is looked up once per device.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_fixed_scratch_mu;
+void *g_fixed_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the fixed scratch array on the current device (looked up on first use).
+tg_status fixed_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+  if (g_fixed_scratch_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_fixed_scratch);
+    if (e != cudaSuccess) return record_cuda(e);
+    g_fixed_scratch_ptr[dev] = ptr;
+  }
+  *out = g_fixed_scratch_ptr[dev];
+  return TG_OK;
+}
+
+}  // namespace
+
+tg_status launch_gated_attention_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                         const float *g, int32_t H_g, const int32_t *cu_kept, int32_t B,
+                                         int32_t M_cap, int32_t max_seqlen, int32_t H_q, int32_t H_kv,
+                                         int32_t d_h, const float *tau, const float *beta, uint16_t *O,
+                                         int32_t *status, cudaStream_t stream) {
+  if (M_cap == 0 || max_seqlen == 0) return TG_OK;
+  const size_t need = gated_attention_workspace_size(B, max_seqlen, H_q, H_kv, d_h);
+  if (need > kFixedScratchBytes) return TG_ERR_UNSUPPORTED;  // more than the fixed array holds
+  void *scratch = nullptr;
+  if (need > 0) {
+    const tg_status st = fixed_scratch(&scratch);
+    if (st != TG_OK) return st;
+    // the array keeps the previous call's contents: its arrival counters must start at zero
+    const int32_t pairs = H_q / (((H_q / H_kv) % 2 == 0) ? 2 : 1);
+    const cudaError_t e =
+        cudaMemsetAsync(scratch, 0, count_bytes(B, pairs, (max_seqlen + kBlockM - 1) / kBlockM), stream);
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  return launch_gated_attention(Q, K, V, g, H_g, cu_kept, B, M_cap, max_seqlen, H_q, H_kv, d_h, tau, beta, O,
+                                status, stream, nullptr, scratch, need > 0 ? kFixedScratchBytes : 0);
 }
 
 }  // namespace tg_host
