@@ -502,6 +502,35 @@ def cpu_baseline(wl, K, min_s=10.0, max_steps=3):
 # main
 # ---------------------------------------------------------------------------
 
+def graph_timed(fn, reps, torch, flush, unit_scale=1000.0):
+    """Median device time of fn's kernels: fn is captured once in a CUDA graph, then each rep
+    flushes L2 and replays the graph between two events on the launching stream, so host
+    launch overhead never lands inside the events. unit_scale 1000 gives microseconds."""
+    fn()  # first call outside capture (sets kernel attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        graph.capture_begin(capture_error_mode="relaxed")
+        fn()
+        graph.capture_end()
+    torch.cuda.current_stream().wait_stream(stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * unit_scale)
+    del graph
+    return float(np.median(ts))
+
+
 def long_context(torch, flush, steps):
     """The 128K long-context workload: one pruned step (K = 8192) against full causal GQA
     attention over all 131,584 tokens, the attention the layers at or below the gate run."""
@@ -570,18 +599,7 @@ def paper_form(path, torch, flush, steps):
                                max_seqlen=path.max_seqlen, b=path.g_kept[:path.M], status=path.status)
 
     def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(3, min(steps, 20))):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1000.0)
-        return float(np.median(ts))
+        return graph_timed(fn, max(3, min(steps, 20)), torch, flush, 1000.0)
 
     # LN_2 fused into scoring: the bench's h stands for the raw residual a^L
     ln_w = torch.from_numpy(np.ascontiguousarray(
@@ -602,7 +620,7 @@ def paper_form(path, torch, flush, steps):
     return {"normalize_scores_us": norm_us, "attention_eq8_us": attn_us,
             "attention_eq8_tflops": flops / (attn_us * 1e-6) / 1e12,
             "gate_score_us": plain_us, "gate_score_rmsnorm_us": fused_us,
-            "note": "single launches with events around each (launch gap included), L2 flushed before each"}
+            "note": "each call captured in a CUDA graph and replayed between events after an L2 flush (median)"}
 
 
 def two_budget(path, torch, flush, steps):
@@ -634,18 +652,7 @@ def two_budget(path, torch, flush, steps):
                            g=path.g, status=path.status)  # the full budget's attention
 
     def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(3, min(steps, 10))):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
+        return graph_timed(fn, max(3, min(steps, 10)), torch, flush, 1.0)
 
     p_ms, s_ms = timed(packed), timed(separate)
     assert tg.read_device_status(path.status) == 0, "device reported an error"
@@ -654,7 +661,7 @@ def two_budget(path, torch, flush, steps):
     return {"K_full": "all document tokens", "K_prune": path.K, "packed_rows": M,
             "packed_ms": p_ms, "separate_ms": s_ms,
             "note": "one scoring pass + one attention call over the 2B-sequence pack, vs the pruned step plus "
-                    "a separate full-budget attention call; host launches inside the events"}
+                    "a separate full-budget attention call; each captured in a CUDA graph, replayed after an L2 flush"}
 
 
 def backward(path, torch, flush, steps):
@@ -685,18 +692,7 @@ def backward(path, torch, flush, steps):
         tg.gate_score_grad(dbias, path.beta, g_kept, path.kept[:M], path.cu_kept, ds)
 
     def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(3, min(steps, 10))):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1000.0)
-        return float(np.median(ts))
+        return graph_timed(fn, max(3, min(steps, 10)), torch, flush, 1000.0)
 
     f_us, b_us, c_us = timed(fwd), timed(bwd), timed(chain)
     assert tg.read_device_status(path.status) == 0, "device reported an error"
@@ -706,8 +702,8 @@ def backward(path, torch, flush, steps):
     torch.cuda.empty_cache()
     return {"forward_lse_us": f_us, "attention_bwd_us": b_us, "gate_score_grad_us": c_us,
             "attention_bwd_tflops": bwd_flops / (b_us * 1e-6) / 1e12,
-            "note": "tensor-core backward (row dots, dK/dV pass, dQ pass); single launches with events around each, "
-                    "L2 flushed before each"}
+            "note": "tensor-core backward (row dots, dK/dV pass, dQ pass); each call captured in a CUDA graph and "
+                    "replayed between events after an L2 flush (median)"}
 
 
 def heads(path, torch, flush, steps):
@@ -739,23 +735,12 @@ def heads(path, torch, flush, steps):
                            max_seqlen=path.max_seqlen, g=path.g_kept, status=path.status)
 
     def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(3, min(steps, 20))):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1000.0)
-        return float(np.median(ts))
+        return graph_timed(fn, max(3, min(steps, 20)), torch, flush, 1000.0)
 
     path.step()  # cu_kept and g_kept for the kept rows
     out = {"H_g": H_g, "gate_score_heads_us": timed(score_heads), "gate_score_us": timed(score_one),
            "attention_per_head_gates_us": timed(attn_heads), "attention_shared_gate_us": timed(attn_one),
-           "note": "single launches with events around each (launch gap included), L2 flushed before each"}
+           "note": "each call captured in a CUDA graph and replayed between events after an L2 flush (median)"}
     assert tg.read_device_status(path.status) == 0, "device reported an error"
     return out
 
