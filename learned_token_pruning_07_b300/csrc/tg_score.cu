@@ -2,39 +2,48 @@
 //
 //   u = W1 h_j (+ b1),  s_j = w2 . SiLU(u) (+ b2),  g_j = sigmoid(s_j)  (g = 1 on non-prunable rows)
 //
-// Persistent kernel: one CTA per SM, each walking 128-row tiles of h (tile = blockIdx.x +
-// k * gridDim.x). Every CTA stages its own h tile and its own W1 slice through TMA; no CTA
-// reads another's shared memory or signals another's barriers. The d_g-wide hidden layer of a
-// tile is computed as n_items column
-// slices of at most 256 (two slices of 256 at d_g = 512). Each slice is one work item: a
-// d-reduction u_slice = h_tile W1_slice^T on the tensor cores (tcgen05.mma kind::f16, bf16
-// operands staged by TMA into 128-byte-swizzled shared memory, fp32 accumulator in one of
-// two 256-column tensor-memory buffers). The epilogue of item i (SiLU, the w2 dot, and at a
-// tile's last slice the sigmoid) runs while the tensor cores already work on item i+1 in the
-// other buffer. A row's partial w2 dots of its slices are summed in registers by the same
-// thread, in slice order, so s is deterministic and no scratch memory is needed.
+// Persistent kernel on CTA pairs (clusters of two, one CTA per SM): a pair walks 256-row tiles
+// of h (pair tile = pair index + k * pairs). The d_g-wide hidden layer of a tile is computed as
+// n_items column slices of at most 256 (two slices of 256 at d_g = 512). Each slice is one work
+// item: a d-reduction u_slice = h_tile W1_slice^T issued as 2-SM tensor-core MMAs
+// (tcgen05.mma.cta_group::2 kind::f16, M = 256): CTA r of the pair stages its own 128 rows of the
+// h tile and its half (rows r * item_n / 2 ..) of the W1 slice, and the tensor cores of the two
+// SMs share the W1 halves, so each SM takes in 32 KB per K-stage of 64 instead of 48 KB. (With
+// every SM loading at once, shared memory fills at about 60 B/clk per SM on this part, under the
+// 94 B/clk that one-CTA 128 x 256 tiles would need to keep their MMAs busy.) The accumulator of
+// a CTA's 128 rows is in its own tensor memory, in one of two 256-column buffers: the epilogue of
+// item i (SiLU, the w2 dot, and at a tile's last slice the sigmoid) runs while the tensor cores
+// already work on item i+1 in the other buffer. A row's partial w2 dots of its slices are summed
+// in registers by the same thread, in slice order, so s is deterministic and no scratch memory
+// is needed.
 //
-// Warp roles: warp 0 lane 0 issues TMA; warp 1 owns tensor memory and issues MMAs (the warp runs
-// converged and one elected lane issues);
-// warps 2-5 run the epilogue (warp w reads tensor-memory lanes 32*(w%4) .. +31, one row per
-// thread). Every wait is bounded (see tg_set_wait_limit_ns); a wait that gives up sets
+// Warp roles: warp 0 lane 0 of each CTA issues that CTA's TMA loads, which complete on the
+// leader's (rank 0's) stage barrier; warp 1 owns tensor memory (allocated for the pair), and in
+// the leader issues the MMAs (the warp runs converged and one elected lane issues) and commits
+// their completion to the barriers of both CTAs; warps 2-5 run the epilogue (warp w reads
+// tensor-memory lanes 32*(w%4) .. +31, one row per thread) and report a drained accumulator to
+// the leader. Every wait is bounded (see tg_set_wait_limit_ns); a wait that gives up sets
 // TG_DEV_TIMEOUT, drains the copies and MMAs in flight, frees tensor memory and returns.
+#include <mutex>
+#include <vector>
+
 #include "tg_common.cuh"
 
 namespace {
 
 constexpr int kBM = 128;      // rows per tile = tensor-memory lanes
 constexpr int kBK = 64;       // d-elements per pipeline stage (one 128-byte swizzled row)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;      // warps 0 (TMA), 1 (MMA), 2-5 (epilogue)
 constexpr int kThreadsNorm = 320;  // + warps 6-9: row sums of squares for the fused RMSNorm
 constexpr int kMaxDg = 512;
 constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
 constexpr int kMaxGateHeads = 16;
+constexpr int kPair = 2;  // CTAs of a cluster: the two halves (128 rows each) of a 256-row tile
 
 struct ScoreParams {
-  int32_t T, d, d_g, n_items, item_n, n_tiles, KT;
+  int32_t T, d, d_g, n_items, item_n, n_tiles, KT;  // n_tiles: 256-row pair tiles
   float ln_eps;  // fused RMSNorm (LN_2 of the residual): 1 / sqrt(mean(h^2) + ln_eps) per row
   const float *b1;
   const uint16_t *w2;  // [H_g, d_g] (one row per gate head)
@@ -59,7 +68,7 @@ struct SmemLayout {
 __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   SmemLayout L;
   L.a_bytes = kBM * kBK * 2;                               // 16 KB
-  L.b_bytes = static_cast<uint32_t>(item_n) * kBK * 2;     // <= 32 KB, a multiple of 1 KB
+  L.b_bytes = static_cast<uint32_t>(item_n / kPair) * kBK * 2;  // this CTA's half: <= 16 KB
   L.off_b = kStages * L.a_bytes;
   L.off_w2 = L.off_b + kStages * L.b_bytes;
   L.off_b1 = L.off_w2 + (ghp == 1 ? kMaxDg * 4 : kMaxDg * ghp * 2);
@@ -69,8 +78,67 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   return L;
 }
 
+// ---- the CTA pair: cluster addresses, TMA into this CTA completing on the leader's barrier,
+// 2-SM MMAs, commits to a barrier of either CTA, and the pair's tensor memory ----
+
+// Address of this CTA's shared variable `p` in the shared memory of CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tg::smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void tma_load_2d_to_leader(void *dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                      int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(tg::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma2_bf16_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrival on the barrier at `bar_cluster` (either CTA) once every 2-SM MMA issued so far by
+// the elected lane has completed.
+__device__ __forceinline__ void commit2_elect(uint32_t bar_cluster) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Tensor memory for 2-SM MMAs: a warp of each CTA of the pair runs these together.
+__device__ __forceinline__ void tmem_alloc2(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tg::smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 template <bool NORM, int GHP>
-__global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
+__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -97,16 +165,19 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  uint32_t rank;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      tg::mbar_init(&full[i], 1);
-      // one MMA commit (+ this CTA's four norm warps)
+      tg::mbar_init(&full[i], 1);  // the leader's: its own expect_tx, the bytes of both CTAs
+      // one MMA commit from the leader (+ this CTA's four norm warps)
       tg::mbar_init(&empty[i], 1 + (NORM ? 4 : 0));
     }
     for (int i = 0; i < 2; ++i) {
       tg::mbar_init(&acc_full[i], 1);
-      tg::mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
+      tg::mbar_init(&acc_empty[i], 4 * kPair);  // the leader's: every epilogue warp of both CTAs
     }
     tg::mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
@@ -121,8 +192,8 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     tg::prefetch_tensormap(&tm_w);
   }
   if (warp == 1) {
-    tg::tmem_alloc(tmem_slot, kTmemCols);
-    tg::tmem_relinquish();
+    tmem_alloc2(tmem_slot, kTmemCols);
+    tmem_relinquish2();
   }
   tg::pdl_wait();
   tg::pdl_launch_dependents();
@@ -140,19 +211,30 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
   tg::tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
   tg::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int32_t *vabort = abort_flag;
-  const uint32_t stage_bytes = L.a_bytes + L.b_bytes;
-  const int tile0 = blockIdx.x;
-  const int tile_stride = gridDim.x;
+  // The 2-SM MMAs write the peer's accumulator at the leader's address: the pair's allocations
+  // must agree (otherwise no work is done and the launch reports TG_DEV_TIMEOUT).
+  bool tmem_ok;
+  {
+    uint32_t other;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(other) : "r"(cluster_addr(tmem_slot, rank ^ 1u)));
+    tmem_ok = other == tmem;
+    if (!tmem_ok && threadIdx.x == 0) *vabort = 1;
+  }
+  // both halves of every stage land on the leader's full barrier
+  const uint32_t stage_bytes = kPair * (L.a_bytes + L.b_bytes);
+  const int tile0 = blockIdx.x / kPair;
+  const int tile_stride = gridDim.x / kPair;
+  const int half_n = p.item_n / kPair;  // W1 rows of a slice this CTA stages
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer: stage = h tile [128 x 64] + W1 slice [item_n x 64] ----
       int kc = 0;
-      bool ok = !p.withhold;
+      bool ok = tmem_ok && !p.withhold;
       for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
         for (int item = 0; item < p.n_items && ok; ++item) {
           for (int kt = 0; kt < p.KT; ++kt, ++kc) {
@@ -162,23 +244,30 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
               ok = false;
               break;
             }
-            // this stage receives the h tile and the W1 slice, both for this CTA alone
-            tg::mbar_arrive_expect_tx(&full[st], stage_bytes);
-            tg::tma_load_2d(sA + st * L.a_bytes, &tm_h, &full[st], kt * kBK, tile * kBM);
-            tg::tma_load_2d(sB + st * L.b_bytes, &tm_w, &full[st], kt * kBK, item * p.item_n);
+            // this CTA's 128 rows of the 256-row h tile and its half of the W1 slice, completing on
+            // the leader's barrier (the leader announces the bytes of both CTAs)
+            if (leader) tg::mbar_arrive_expect_tx(&full[st], stage_bytes);
+            const uint32_t bar = cluster_addr(&full[st], 0);
+            tma_load_2d_to_leader(sA + st * L.a_bytes, &tm_h, bar, kt * kBK, tile * (kPair * kBM) + rank * kBM);
+            tma_load_2d_to_leader(sB + st * L.b_bytes, &tm_w, bar, kt * kBK, item * p.item_n + rank * half_n);
             *n_issued = kc + 1;
           }
         }
       }
+      // tail: the leader's last commits to this CTA's stage barriers have landed before it exits
+      for (int k = kc - kStages < 0 ? 0 : kc - kStages; ok && k < kc; ++k)
+        ok = tg::mbar_wait(&empty[k % kStages], (k / kStages) & 1, vabort, p.wait_limit);
+      if (!ok) *vabort = 1;
     }
   } else if (warp == 1) {
-    {
-      // ---- MMA issuer (converged warp, elected lane): u_slice[128 x item_n] += A[128 x 16] * B[item_n x 16]^T ----
-      const uint32_t idesc = tg::idesc_bf16_f32(kBM, p.item_n);
+    if (leader) {
+      // ---- MMA issuer (converged warp, elected lane):
+      //      u_slice[256 x item_n] += A[256 x 16] * B[item_n x 16]^T over the pair ----
+      const uint32_t idesc = tg::idesc_bf16_f32(kPair * kBM, p.item_n);
       const uint64_t a0 = tg::smem_desc(tg::smem_u32(sA), 16, 1024, tg::kSwz128);
       const uint64_t b0 = tg::smem_desc(tg::smem_u32(sB), 16, 1024, tg::kSwz128);
       int kc = 0, it = 0;
-      bool ok = true;
+      bool ok = tmem_ok;
       for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
         for (int item = 0; item < p.n_items && ok; ++item, ++it) {
           const int buf = it & 1;
@@ -194,21 +283,28 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
               ok = false;
               break;
             }
+            // the peer's norm warps learn here that its half of the stage has landed
+            if (NORM && lane == 0) mbar_arrive_cluster(cluster_addr(&full[st], 1));
             tg::tc_fence_after();
             const uint64_t ad = a0 + ((st * L.a_bytes) >> 4), bd = b0 + ((st * L.b_bytes) >> 4);
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)  // a K-step of 16 is 32 bytes into the 128-byte row
-              tg::mma_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
-            tg::mma_commit_elect(&empty[st]);  // the stage is free once these MMAs have read it
+              mma2_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
+            // the stage is free in both CTAs once these MMAs have read it
+            commit2_elect(cluster_addr(&empty[st], 0));
+            commit2_elect(cluster_addr(&empty[st], 1));
             if (lane == 0) *n_consumed = kc + 1;
           }
-          if (ok) tg::mma_commit_elect(&acc_full[buf]);
+          if (ok) {
+            commit2_elect(cluster_addr(&acc_full[buf], 0));
+            commit2_elect(cluster_addr(&acc_full[buf], 1));
+          }
         }
       }
       if (!ok) {
         *vabort = 1;
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
-        tg::mma_commit_elect(drain);
+        commit2_elect(cluster_addr(drain, 0));
         volatile int32_t never = 0;
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
@@ -219,7 +315,7 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0, ti = 0;
-    bool ok = true;
+    bool ok = tmem_ok;
     for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
       float acc[GHP];
 #pragma unroll
@@ -279,7 +375,10 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
         }
         tg::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tg::mbar_arrive(&acc_empty[buf]);
+        if (lane == 0) {  // the leader's MMAs may reuse this buffer in both CTAs
+          if (leader) tg::mbar_arrive(&acc_empty[buf]);
+          else mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
+        }
       }
       if (!ok) break;
       if constexpr (GHP > 1) {
@@ -291,7 +390,7 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
         __syncwarp();
         if (lane == 0) tg::mbar_arrive(&rms_free[ti & 1]);  // this tile's 1/rms slots are free
       }
-      const int row = tile * kBM + r;
+      const int row = tile * (kPair * kBM) + static_cast<int>(rank) * kBM + r;
       if (row < p.T) {
         const bool keep_always = p.mask && p.mask[row];
         if (GHP == 1) {
@@ -322,7 +421,7 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     // Row r of a 128-byte-swizzled stage holds its eight 16-byte chunks at positions c ^ (r % 8).
     const int r = (warp - 6) * 32 + lane;
     int kc = 0, ti = 0;
-    bool ok = true;
+    bool ok = tmem_ok;
     for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
       float sq = 0.0f;
       for (int item = 0; item < p.n_items && ok; ++item) {
@@ -365,16 +464,21 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
   if (*vabort) {
     if (threadIdx.x == 0) {
       tg::report(p.status, TG_DEV_TIMEOUT);
-      // wait (bounded) for TMA copies that were issued but never consumed
+      // wait (bounded) for TMA copies that were issued but never consumed; the copies of both
+      // CTAs complete on the leader's barriers
       volatile int32_t never = 0;
-      for (int i = *n_consumed; i < *n_issued; ++i)
-        tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.drain_limit);
+      if (leader)
+        for (int i = *n_consumed; i < *n_issued; ++i)
+          tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.drain_limit);
     }
     __syncthreads();
   }
+  // no CTA of the pair frees tensor memory or exits while the other may still arrive on its
+  // barriers or run MMAs into its tensor memory
+  cluster_sync_all();
   if (warp == 1) {
     tg::tc_fence_after();
-    tg::tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc2(tmem, kTmemCols);
   }
 }
 
@@ -383,6 +487,46 @@ __global__ void __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
 namespace tg_host {
 
 namespace {
+
+// CTA pairs that are resident at once for this kernel and shared-memory size (cached per
+// device, kernel and size; at least one).
+cudaError_t resident_pairs(const void *kernel, int threads, size_t smem, int *pairs) {
+  struct Entry {
+    int dev;
+    const void *kernel;
+    size_t smem;
+    int pairs;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry &c : cache)
+    if (c.dev == dev && c.kernel == kernel && c.smem == smem) {
+      *pairs = c.pairs;
+      return cudaSuccess;
+    }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kPair * num_sms());
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) n = 1;
+  cache.push_back({dev, kernel, smem, n});
+  *pairs = n;
+  return cudaSuccess;
+}
 
 template <bool NORM>
 decltype(&gate_score_kernel<NORM, 1>) score_kernel_for(int ghp) {
@@ -415,7 +559,7 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   p.ln_eps = ln_eps;
   p.n_items = d_g > kMaxItemN ? 2 : 1;
   p.item_n = d_g / p.n_items;  // d_g % 32 == 0, so a multiple of 16, at most 256
-  p.n_tiles = (T + kBM - 1) / kBM;
+  p.n_tiles = (T + kPair * kBM - 1) / (kPair * kBM);
   p.KT = (d + kBK - 1) / kBK;  // a ragged last stage reads zeros past d from both operands
   p.b1 = b1;
   p.w2 = w2;
@@ -439,18 +583,21 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(d_g)};
     const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.item_n)};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(p.item_n / kPair)};  // one CTA's half of a slice
     if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
   const SmemLayout L = score_smem_layout(p.item_n, ghp);
-  int ctas = num_sms();
-  if (ctas > p.n_tiles) ctas = p.n_tiles;
   auto kernel = rmsnorm ? score_kernel_for<true>(ghp) : score_kernel_for<false>(ghp);
+  const int threads = rmsnorm ? kThreadsNorm : kThreads;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
-  return record_cuda(launch_pdl(kernel, dim3(ctas), dim3(rmsnorm ? kThreadsNorm : kThreads),
-                                L.total, stream, tm_h, tm_w, p));
+  // one wave of pairs: as many as fit at once (a pair sits in one GPC, so an odd SM is left out)
+  int pairs = 0;
+  e = resident_pairs(reinterpret_cast<const void *>(kernel), threads, L.total, &pairs);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (pairs > p.n_tiles) pairs = p.n_tiles;
+  return record_cuda(launch_pdl(kernel, dim3(kPair * pairs), dim3(threads), L.total, stream, tm_h, tm_w, p));
 }
 
 // ---------------------------------------------------------------------------
