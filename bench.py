@@ -773,7 +773,7 @@ def select_gather_summary(work, stages, peaks):
             "frac": by / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
 
 
-def other_configs(torch, flush, steps, peaks, rank):
+def other_configs(torch, flush, steps, peaks, rank, with_oracle=True):
     """Throughput lines of the other single-GPU workloads: the Qwen3-1.7B-shaped 8K gate layer
     (K = 1024) and the ragged batch of eight sequences (K = 2048 each, selection on 256-level
     scores), each with its per-kernel times and roofline fractions."""
@@ -790,13 +790,20 @@ def other_configs(torch, flush, steps, peaks, rank):
         work = stage_work(wl, wl.K, p.kept_lens)
         st = stage_summary(work, pst, peaks)
         ms = float(ps.mean())
-        out.append({"workload": workload_label(base, wl.K), "K": wl.K, "T_total": wl.T_total, "M_kept": p.M,
-                    "value": wl.T_total / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "stages": st,
-                    "select_plus_gather": select_gather_summary(work, st, peaks),
-                    "selection_scores": ("synthetic 256-level quantised buffer" if wl.score_levels
-                                         else "the step's own gate scores")})
+        entry = {"workload": workload_label(base, wl.K), "K": wl.K, "T_total": wl.T_total, "M_kept": p.M,
+                 "value": wl.T_total / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "stages": st,
+                 "select_plus_gather": select_gather_summary(work, st, peaks),
+                 "selection_scores": ("synthetic 256-level quantised buffer" if wl.score_levels
+                                      else "the step's own gate scores")}
         del g, p
         torch.cuda.empty_cache()
+        if with_oracle:
+            # one whole, unsampled oracle step of the same workload on the host cores
+            t = oracle_step(base, base.K, {})
+            entry["cpu_oracle"] = {"value": base.T_total / t["step"], "unit": UNIT, "ms_per_step": 1000.0 * t["step"],
+                                   "stage_ms": {k: 1000.0 * v for k, v in t.items()}, "cores": blas_threads(),
+                                   "kind": "oracle", "sample": oracle_sample_text(1, t["step"])}
+        out.append(entry)
     return out
 
 
@@ -934,7 +941,8 @@ def run_gpu(args, rank, world, local):
                 torch.cuda.empty_cache()
 
     extras = rank == 0 and args.extras
-    others = other_configs(torch, flush, args.steps, peaks, rank) if (rank == 0 and args.configs) else None
+    others = (other_configs(torch, flush, args.steps, peaks, rank, with_oracle=world == 1 and not args.no_cpu_baseline)
+              if (rank == 0 and args.configs) else None)
     paper = paper_form(path, torch, flush, args.steps) if extras else None
     twob = two_budget(path, torch, flush, args.steps) if extras else None
     bwd = backward(path, torch, flush, args.steps) if extras else None
