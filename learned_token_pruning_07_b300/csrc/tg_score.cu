@@ -33,7 +33,9 @@ namespace {
 
 constexpr int kBM = 128;      // rows per tile = tensor-memory lanes
 constexpr int kBK = 64;       // d-elements per pipeline stage (one 128-byte swizzled row)
-constexpr int kStages = 6;
+// Pipeline stages: 7 with one gate head (b1 and w2 are then read through L1, leaving shared
+// memory to the stages), 6 with several (their W2 table stays in shared memory).
+__host__ __device__ constexpr int stages_for(int ghp) { return ghp == 1 ? 7 : 6; }
 constexpr int kThreads = 192;      // warps 0 (TMA), 1 (MMA), 2-5 (epilogue)
 constexpr int kThreadsNorm = 320;  // + warps 6-9: row sums of squares for the fused RMSNorm
 constexpr int kMaxDg = 512;
@@ -59,20 +61,23 @@ struct ScoreParams {
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
 };
 
+__device__ const float g_zero_b1[kMaxDg] = {};  // b1 of a layer without a first-layer bias
+
 struct SmemLayout {
   uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_rms, off_bar, total;
 };
 
-// ghp: gate heads padded to 1, 2, 4, 8 or 16. One head keeps w2 as fp32 [d_g]; more heads keep
-// W2 as bf16 pairs [d_g][ghp / 2] (16 KB at 16 heads), zero past H_g.
+// ghp: gate heads padded to 1, 2, 4, 8 or 16. More than one head keeps W2 as bf16 pairs
+// [d_g][ghp / 2] (16 KB at 16 heads, zero past H_g) and b1 as fp32 [d_g] in shared memory.
 __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   SmemLayout L;
+  const int S = stages_for(ghp);
   L.a_bytes = kBM * kBK * 2;                               // 16 KB
   L.b_bytes = static_cast<uint32_t>(item_n / kPair) * kBK * 2;  // this CTA's half: <= 16 KB
-  L.off_b = kStages * L.a_bytes;
-  L.off_w2 = L.off_b + kStages * L.b_bytes;
-  L.off_b1 = L.off_w2 + (ghp == 1 ? kMaxDg * 4 : kMaxDg * ghp * 2);
-  L.off_rms = L.off_b1 + kMaxDg * 4;           // [2 tiles][128 rows] fp32 1 / rms
+  L.off_b = S * L.a_bytes;
+  L.off_w2 = L.off_b + S * L.b_bytes;
+  L.off_b1 = L.off_w2 + (ghp == 1 ? 0 : kMaxDg * ghp * 2);
+  L.off_rms = L.off_b1 + (ghp == 1 ? 0 : kMaxDg * 4);  // [2 tiles][128 rows] fp32 1 / rms
   L.off_bar = L.off_rms + 2 * kBM * 4;
   L.total = L.off_bar + 256 + 1024;  // barriers + slots, plus alignment slack
   return L;
@@ -137,6 +142,47 @@ __device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Epilogue of NC accumulator columns of one row (hidden units hid .. hid + NC - 1): u = the
+// accumulator (times 1 / rms under the fused RMSNorm) + b1, then w2 . SiLU(u) into acc (one
+// head) or, per head pair, into the packed fp32 pairs acc2, in column order.
+// b1: fp32 [d_g] (global memory with one head, read through L1; shared memory otherwise);
+// w2g: the one head's bf16 w2 [d_g] in global memory; s_w2h: the heads' bf16 pairs in shared memory.
+template <int NC, bool NORM, int GHP>
+__device__ __forceinline__ void score_chunk(const uint32_t (&v)[NC], int hid, float inv_rms, const float *b1,
+                                            const uint16_t *w2g, const uint32_t *s_w2h, float *acc, uint64_t *acc2) {
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const float bias = GHP == 1 ? __ldg(b1 + hid + i) : b1[hid + i];
+    const float u = NORM ? fmaf(__uint_as_float(v[i]), inv_rms, bias) : __uint_as_float(v[i]) + bias;
+    const float silu = __fdividef(u, 1.0f + __expf(-u));
+    if constexpr (GHP == 1) {
+      acc[0] = fmaf(tg::bf16_bits_to_float(__ldg(w2g + hid + i)), silu, acc[0]);
+    } else {
+      // every thread reads the same column's weights: a shared-memory broadcast
+      uint32_t w[GHP / 2];
+      const uint32_t *src = s_w2h + (hid + i) * (GHP / 2);
+      if constexpr (GHP >= 8) {
+#pragma unroll
+        for (int k = 0; k < GHP / 2; k += 4) {
+          const uint4 q = *reinterpret_cast<const uint4 *>(src + k);
+          w[k] = q.x; w[k + 1] = q.y; w[k + 2] = q.z; w[k + 3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < GHP / 2; ++k) w[k] = src[k];
+      }
+      uint64_t silu2;
+      asm("mov.b64 %0, {%1, %1};" : "=l"(silu2) : "f"(silu));
+#pragma unroll
+      for (int k = 0; k < GHP / 2; ++k) {
+        uint64_t wk;  // the bf16 pair widened to fp32: low half, then high half
+        asm("mov.b64 %0, {%1, %2};" : "=l"(wk) : "r"(w[k] << 16), "r"(w[k] & 0xFFFF0000u));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[k]) : "l"(wk), "l"(silu2));
+      }
+    }
+  }
+}
+
 template <bool NORM, int GHP>
 __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
@@ -147,10 +193,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   const SmemLayout L = score_smem_layout(p.item_n, GHP);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
-  float *s_w2 = reinterpret_cast<float *>(smem + L.off_w2);
   uint32_t *s_w2h = reinterpret_cast<uint32_t *>(smem + L.off_w2);  // GHP > 1: [d_g][GHP / 2] bf16 pairs
   float *s_b1 = reinterpret_cast<float *>(smem + L.off_b1);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
+  constexpr int kStages = stages_for(GHP);
   uint64_t *empty = full + kStages;
   uint64_t *acc_full = empty + kStages;  // [2] MMA -> epilogue
   uint64_t *acc_empty = acc_full + 2;    // [2] epilogue -> MMA
@@ -197,19 +243,19 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   }
   tg::pdl_wait();
   tg::pdl_launch_dependents();
-  for (int i = threadIdx.x; i < p.d_g; i += blockDim.x) {
-    if (GHP == 1) {
-      s_w2[i] = tg::bf16_bits_to_float(p.w2[i]);
-    } else {
+  if constexpr (GHP > 1) {
+    for (int i = threadIdx.x; i < p.d_g; i += blockDim.x) {
 #pragma unroll
       for (int k = 0; k < GHP / 2; ++k) {
         const uint32_t lo = 2 * k < p.H_g ? p.w2[static_cast<size_t>(2 * k) * p.d_g + i] : 0u;
         const uint32_t hi = 2 * k + 1 < p.H_g ? p.w2[static_cast<size_t>(2 * k + 1) * p.d_g + i] : 0u;
         s_w2h[i * (GHP / 2) + k] = lo | (hi << 16);
       }
+      s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
     }
-    s_b1[i] = p.b1 ? p.b1[i] : 0.0f;
   }
+  // one head: b1 (or zeros) and w2 straight from global memory
+  const float *b1_src = GHP == 1 ? (p.b1 ? p.b1 : g_zero_b1) : s_b1;
   tg::tc_fence_before();
   cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
   tg::tc_fence_after();
@@ -335,43 +381,22 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
         ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_full[buf], (it >> 1) & 1, vabort, p.wait_limit));
         if (!ok) break;
         tg::tc_fence_after();
-        const uint32_t col0 = static_cast<uint32_t>(buf * kMaxItemN);
+        const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * kMaxItemN);
         const int hid0 = item * p.item_n;
-        for (int c0 = 0; c0 < p.item_n; c0 += 32) {
+        // 32-column chunks; a slice width that is an odd multiple of 16 ends with a 16-column
+        // chunk (a 32-column load there would take in the next slice's columns)
+        const int n32 = p.item_n >> 5;
+        for (int c = 0; c < n32; ++c) {
           uint32_t v[32];
-          tg::tmem_ld_32x32b_x32(lane_base + col0 + c0, v);
+          tg::tmem_ld_32x32b_x32(taddr + c * 32, v);
           tg::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float u = NORM ? fmaf(__uint_as_float(v[i]), inv_rms, s_b1[hid0 + c0 + i])
-                                 : __uint_as_float(v[i]) + s_b1[hid0 + c0 + i];
-            const float silu = __fdividef(u, 1.0f + __expf(-u));
-            if constexpr (GHP == 1) {
-              acc[0] = fmaf(s_w2[hid0 + c0 + i], silu, acc[0]);
-            } else {
-              // every thread reads the same column's weights: a shared-memory broadcast
-              uint32_t w[GHP / 2];
-              const uint32_t *src = s_w2h + (hid0 + c0 + i) * (GHP / 2);
-              if constexpr (GHP >= 8) {
-#pragma unroll
-                for (int k = 0; k < GHP / 2; k += 4) {
-                  const uint4 q = *reinterpret_cast<const uint4 *>(src + k);
-                  w[k] = q.x; w[k + 1] = q.y; w[k + 2] = q.z; w[k + 3] = q.w;
-                }
-              } else {
-#pragma unroll
-                for (int k = 0; k < GHP / 2; ++k) w[k] = src[k];
-              }
-              uint64_t silu2;
-              asm("mov.b64 %0, {%1, %1};" : "=l"(silu2) : "f"(silu));
-#pragma unroll
-              for (int k = 0; k < GHP / 2; ++k) {
-                uint64_t wk;  // the bf16 pair widened to fp32: low half, then high half
-                asm("mov.b64 %0, {%1, %2};" : "=l"(wk) : "r"(w[k] << 16), "r"(w[k] & 0xFFFF0000u));
-                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[k]) : "l"(wk), "l"(silu2));
-              }
-            }
-          }
+          score_chunk<32, NORM, GHP>(v, hid0 + c * 32, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
+        }
+        if (p.item_n & 16) {
+          uint32_t vt[16];
+          tg::tmem_ld_32x32b_x16(taddr + n32 * 32, vt);
+          tg::tmem_ld_wait();
+          score_chunk<16, NORM, GHP>(vt, hid0 + n32 * 32, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
         }
         tg::tc_fence_before();
         __syncwarp();

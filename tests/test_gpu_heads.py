@@ -94,6 +94,13 @@ def test_score_heads_ragged_tail_two_slices():
     _score_heads(wl, 8)
 
 
+def test_score_heads_slices_of_an_odd_multiple_of_16():
+    # d_g = 480: two slices of 240 columns, each ending with a 16-column chunk
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(700,), instr_lens=(9,), d=256, d_g=480)
+    _score_heads(wl, 4)
+    _score_heads(wl, 16, rmsnorm=True)
+
+
 def test_score_heads_qwen3_gate_layer_8k():
     _score_heads(I.WORKLOADS["qwen3_1p7b_8k"], 16)
 

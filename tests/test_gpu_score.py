@@ -47,6 +47,15 @@ def test_score_ragged_tail_and_bias():
     _score(wl, b1=b1, b2=-0.25)
 
 
+@pytest.mark.parametrize("d_g", [288, 480])
+def test_score_slices_of_an_odd_multiple_of_16(d_g):
+    # d_g > 256 splits into two slices of d_g / 2 = 144 or 240 columns: each ends with a
+    # 16-column chunk, which must not pick up the next slice's columns; T spans 3 pair tiles
+    wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(700,), instr_lens=(9,), d=256, d_g=d_g)
+    b1 = np.random.default_rng(d_g).standard_normal(d_g) * 0.5
+    _score(wl, b1=b1, b2=0.125)
+
+
 def test_score_small_dg_no_mask():
     wl = I.with_changes(I.WORKLOADS["tiny"], doc_lens=(130,), instr_lens=(0,), d=64, d_g=32)
     _score(wl, with_mask=False)
@@ -122,6 +131,10 @@ def test_score_rmsnorm_tiny():
 def test_score_rmsnorm_ragged_tail_two_slices():
     _rmsnorm_case(I.with_changes(I.WORKLOADS["tiny"], doc_lens=(900,), instr_lens=(17,), d=512, d_g=384),
                   ln_eps=1e-5)
+
+
+def test_score_rmsnorm_slices_of_an_odd_multiple_of_16():
+    _rmsnorm_case(I.with_changes(I.WORKLOADS["tiny"], doc_lens=(700,), instr_lens=(9,), d=256, d_g=288))
 
 
 def test_score_rmsnorm_qwen3_gate_layer_8k():
