@@ -43,6 +43,10 @@ constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumu
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
 constexpr int kMaxGateHeads = 16;
 constexpr int kPair = 2;  // CTAs of a cluster: the two halves (128 rows each) of a 256-row tile
+// Barrier region: full, empty and landed per stage (at most 7 stages), acc_full[2], acc_empty[2],
+// drain, rms_ready[2], rms_free[2]; then the tensor-memory slot and three int32 flags.
+constexpr uint32_t kBarBytes = 320;
+static_assert((3 * 7 + 9) * 8 + 4 * 4 <= kBarBytes, "barrier region too small");
 
 struct ScoreParams {
   int32_t T, d, d_g, n_items, item_n, n_tiles, KT;  // n_tiles: 256-row pair tiles
@@ -79,7 +83,7 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   L.off_b1 = L.off_w2 + (ghp == 1 ? 0 : kMaxDg * ghp * 2);
   L.off_rms = L.off_b1 + (ghp == 1 ? 0 : kMaxDg * 4);  // [2 tiles][128 rows] fp32 1 / rms
   L.off_bar = L.off_rms + 2 * kBM * 4;
-  L.total = L.off_bar + 256 + 1024;  // barriers + slots, plus alignment slack
+  L.total = L.off_bar + kBarBytes + 1024;  // barriers + slots, plus alignment slack
   return L;
 }
 
@@ -204,7 +208,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   uint64_t *rms_ready = drain + 1;       // [2] norm warps -> epilogue (by tile parity)
   uint64_t *rms_free = rms_ready + 2;    // [2] epilogue -> norm warps
   float *s_inv_rms = reinterpret_cast<float *>(smem + L.off_rms);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rms_free + 2);
+  uint64_t *landed = rms_free + 2;       // [kStages] leader's MMA commit -> the peer's norm warps
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(landed + kStages);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
   int32_t *n_consumed = abort_flag + 2;
@@ -230,6 +235,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       tg::mbar_init(&rms_ready[i], 4);
       tg::mbar_init(&rms_free[i], 4);
     }
+    for (int i = 0; i < kStages; ++i) tg::mbar_init(&landed[i], 1);
     *abort_flag = 0;
     *n_issued = 0;
     *n_consumed = 0;
@@ -329,13 +335,14 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
               ok = false;
               break;
             }
-            // the peer's norm warps learn here that its half of the stage has landed
-            if (NORM && lane == 0) mbar_arrive_cluster(cluster_addr(&full[st], 1));
             tg::tc_fence_after();
             const uint64_t ad = a0 + ((st * L.a_bytes) >> 4), bd = b0 + ((st * L.b_bytes) >> 4);
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)  // a K-step of 16 is 32 bytes into the 128-byte row
               mma2_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
+            // the peer's norm warps may read their half once these MMAs have (a release arrival to
+            // another CTA would cost this thread about 2,000 cycles; a commit costs it nothing)
+            if (NORM) commit2_elect(cluster_addr(&landed[st], 1));
             // the stage is free in both CTAs once these MMAs have read it
             commit2_elect(cluster_addr(&empty[st], 0));
             commit2_elect(cluster_addr(&empty[st], 1));
@@ -452,7 +459,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       for (int item = 0; item < p.n_items && ok; ++item) {
         for (int kt = 0; kt < p.KT; ++kt, ++kc) {
           const int st = kc % kStages;
-          ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&full[st], (kc / kStages) & 1, vabort, p.wait_limit));
+          // the peer's stages complete on the leader's barrier; its norm warps learn that a stage
+          // has landed from the commit of the MMAs that read it
+          ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(leader ? &full[st] : &landed[st], (kc / kStages) & 1, vabort,
+                                                     p.wait_limit));
           if (!ok) break;
           if (item == 0) {  // every slice re-reads the same h tile; the first pass suffices
             const uint4 *row_base = reinterpret_cast<const uint4 *>(sA + st * L.a_bytes + r * 128);
