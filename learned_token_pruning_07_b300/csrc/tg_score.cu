@@ -367,6 +367,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     const int quarter = warp & 3;  // tensor-memory lane quarter this warp may read
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // accumulator units (tile, slice) this pair computes
+    const int n_units = tile0 < p.n_tiles ? ((p.n_tiles - 1 - tile0) / tile_stride + 1) * p.n_items : 0;
     int it = 0, ti = 0;
     bool ok = tmem_ok;
     for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
@@ -407,9 +409,12 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
         }
         tg::tc_fence_before();
         __syncwarp();
-        if (lane == 0) {  // the leader's MMAs may reuse this buffer in both CTAs
+        // the leader's MMAs may reuse this buffer in both CTAs. The MMAs wait for a buffer only
+        // before the unit two ahead, so the last two units need no report; the peer skips them,
+        // since a release arrival to another CTA holds its warp for about 2,000 cycles
+        if (lane == 0) {
           if (leader) tg::mbar_arrive(&acc_empty[buf]);
-          else mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
+          else if (it + 2 < n_units) mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
         }
       }
       if (!ok) break;
