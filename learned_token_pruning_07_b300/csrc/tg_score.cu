@@ -36,17 +36,21 @@ constexpr int kBK = 64;       // d-elements per pipeline stage (one 128-byte swi
 // Pipeline stages: 7 with one gate head (b1 and w2 are then read through L1, leaving shared
 // memory to the stages), 6 with several (their W2 table stays in shared memory).
 __host__ __device__ constexpr int stages_for(int ghp) { return ghp == 1 ? 7 : 6; }
-constexpr int kThreads = 192;      // warps 0 (TMA), 1 (MMA), 2-5 (epilogue)
-constexpr int kThreadsNorm = 320;  // + warps 6-9: row sums of squares for the fused RMSNorm
+// Warps 0 (TMA), 1 (MMA), 2-9: eight epilogue warps (two per tensor-memory lane quarter, each
+// taking half of every slice's columns), or with the fused RMSNorm four epilogue warps (2-5)
+// and four that sum each row's squares (6-9).
+constexpr int kThreads = 320;
+__host__ __device__ constexpr int epi_warps(bool norm) { return norm ? 4 : 8; }
 constexpr int kMaxDg = 512;
 constexpr int kMaxItemN = 256;  // columns of one slice = one MMA N = one accumulator buffer
 constexpr uint32_t kTmemCols = 2 * kMaxItemN;
 constexpr int kMaxGateHeads = 16;
 constexpr int kPair = 2;  // CTAs of a cluster: the two halves (128 rows each) of a 256-row tile
 // Barrier region: full, empty and landed per stage (at most 7 stages), acc_full[2], acc_empty[2],
-// drain, rms_ready[2], rms_free[2]; then the tensor-memory slot and three int32 flags.
+// drain, rms_ready[2], rms_free[2], xch_full[4], xch_free[4]; then the tensor-memory slot and
+// three int32 flags.
 constexpr uint32_t kBarBytes = 320;
-static_assert((3 * 7 + 9) * 8 + 4 * 4 <= kBarBytes, "barrier region too small");
+static_assert((3 * 7 + 9 + 8) * 8 + 4 * 4 <= kBarBytes, "barrier region too small");
 
 struct ScoreParams {
   int32_t T, d, d_g, n_items, item_n, n_tiles, KT;  // n_tiles: 256-row pair tiles
@@ -73,7 +77,7 @@ struct SmemLayout {
 
 // ghp: gate heads padded to 1, 2, 4, 8 or 16. More than one head keeps W2 as bf16 pairs
 // [d_g][ghp / 2] (16 KB at 16 heads, zero past H_g) and b1 as fp32 [d_g] in shared memory.
-__host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
+__host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp, bool norm) {
   SmemLayout L;
   const int S = stages_for(ghp);
   L.a_bytes = kBM * kBK * 2;                               // 16 KB
@@ -81,8 +85,10 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp) {
   L.off_b = S * L.a_bytes;
   L.off_w2 = L.off_b + S * L.b_bytes;
   L.off_b1 = L.off_w2 + (ghp == 1 ? 0 : kMaxDg * ghp * 2);
-  L.off_rms = L.off_b1 + (ghp == 1 ? 0 : kMaxDg * 4);  // [2 tiles][128 rows] fp32 1 / rms
-  L.off_bar = L.off_rms + 2 * kBM * 4;
+  // fused RMSNorm: [2 tiles][128 rows] fp32 1 / rms; otherwise [ghp][128 rows] fp32, the
+  // second-half epilogue warps' partial row sums handed to the first half
+  L.off_rms = L.off_b1 + (ghp == 1 ? 0 : kMaxDg * 4);
+  L.off_bar = L.off_rms + (norm ? 2 * kBM * 4 : kBM * ghp * 4);
   L.total = L.off_bar + kBarBytes + 1024;  // barriers + slots, plus alignment slack
   return L;
 }
@@ -188,13 +194,14 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&v)[NC], int hid, fl
 }
 
 template <bool NORM, int GHP>
-__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsNorm : kThreads, 1)
+__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = score_smem_layout(p.item_n, GHP);
+  const SmemLayout L = score_smem_layout(p.item_n, GHP, NORM);
+  constexpr int EW = epi_warps(NORM);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
   uint32_t *s_w2h = reinterpret_cast<uint32_t *>(smem + L.off_w2);  // GHP > 1: [d_g][GHP / 2] bf16 pairs
@@ -209,7 +216,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
   uint64_t *rms_free = rms_ready + 2;    // [2] epilogue -> norm warps
   float *s_inv_rms = reinterpret_cast<float *>(smem + L.off_rms);
   uint64_t *landed = rms_free + 2;       // [kStages] leader's MMA commit -> the peer's norm warps
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(landed + kStages);
+  uint64_t *xch_full = landed + kStages;  // [4] per lane quarter: second-half partial sums written
+  uint64_t *xch_free = xch_full + 4;      // [4] per lane quarter: the first half has read them
+  float *s_xch = s_inv_rms;               // without the fused RMSNorm: [GHP][128 rows] partial sums
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xch_free + 4);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
   int32_t *n_consumed = abort_flag + 2;
@@ -228,7 +238,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
     }
     for (int i = 0; i < 2; ++i) {
       tg::mbar_init(&acc_full[i], 1);
-      tg::mbar_init(&acc_empty[i], 4 * kPair);  // the leader's: every epilogue warp of both CTAs
+      tg::mbar_init(&acc_empty[i], EW * kPair);  // the leader's: every epilogue warp of both CTAs
     }
     tg::mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
@@ -236,6 +246,10 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       tg::mbar_init(&rms_free[i], 4);
     }
     for (int i = 0; i < kStages; ++i) tg::mbar_init(&landed[i], 1);
+    for (int i = 0; i < 4; ++i) {
+      tg::mbar_init(&xch_full[i], 1);
+      tg::mbar_init(&xch_free[i], 1);
+    }
     *abort_flag = 0;
     *n_issued = 0;
     *n_consumed = 0;
@@ -362,10 +376,15 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + EW) {
     // ---- epilogue: one row per thread; SiLU . w2 over each slice, sigmoid at the end ----
     const int quarter = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int half = (warp - 2) >> 2;  // with eight epilogue warps: which half of the columns
     const int r = quarter * 32 + lane;
+    // this warp's 16-column groups of every slice
+    const int n_g = p.item_n >> 4;
+    const int g0 = (EW == 8 && half == 1) ? n_g / 2 : 0;
+    const int g1 = (EW == 8 && half == 0) ? n_g / 2 : n_g;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     // accumulator units (tile, slice) this pair computes
     const int n_units = tile0 < p.n_tiles ? ((p.n_tiles - 1 - tile0) / tile_stride + 1) * p.n_items : 0;
@@ -392,20 +411,20 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
         tg::tc_fence_after();
         const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * kMaxItemN);
         const int hid0 = item * p.item_n;
-        // 32-column chunks; a slice width that is an odd multiple of 16 ends with a 16-column
-        // chunk (a 32-column load there would take in the next slice's columns)
-        const int n32 = p.item_n >> 5;
-        for (int c = 0; c < n32; ++c) {
+        // 32-column chunks over this warp's groups; an odd group count ends with a 16-column
+        // chunk (a 32-column load there would take in columns that are not this warp's)
+        int g = g0;
+        for (; g + 2 <= g1; g += 2) {
           uint32_t v[32];
-          tg::tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tg::tmem_ld_32x32b_x32(taddr + g * 16, v);
           tg::tmem_ld_wait();
-          score_chunk<32, NORM, GHP>(v, hid0 + c * 32, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
+          score_chunk<32, NORM, GHP>(v, hid0 + g * 16, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
         }
-        if (p.item_n & 16) {
+        if (g < g1) {
           uint32_t vt[16];
-          tg::tmem_ld_32x32b_x16(taddr + n32 * 32, vt);
+          tg::tmem_ld_32x32b_x16(taddr + g * 16, vt);
           tg::tmem_ld_wait();
-          score_chunk<16, NORM, GHP>(vt, hid0 + n32 * 32, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
+          score_chunk<16, NORM, GHP>(vt, hid0 + g * 16, inv_rms, b1_src, p.w2, s_w2h, acc, acc2);
         }
         tg::tc_fence_before();
         __syncwarp();
@@ -426,6 +445,25 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(NORM ? kThreadsN
       if (NORM) {
         __syncwarp();
         if (lane == 0) tg::mbar_arrive(&rms_free[ti & 1]);  // this tile's 1/rms slots are free
+      }
+      if constexpr (EW == 8) {
+        // the second half hands its partial sums to the first, which adds them after its own
+        // (a fixed order, so s does not depend on timing) and writes the row's results
+        if (half == 1) {
+          ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&xch_free[quarter], (ti & 1) ^ 1u, vabort, p.wait_limit));
+          if (!ok) break;
+#pragma unroll
+          for (int c = 0; c < GHP; ++c) s_xch[c * kBM + r] = acc[c];
+          __syncwarp();
+          if (lane == 0) tg::mbar_arrive(&xch_full[quarter]);
+          continue;
+        }
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&xch_full[quarter], ti & 1, vabort, p.wait_limit));
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < GHP; ++c) acc[c] += s_xch[c * kBM + r];
+        __syncwarp();
+        if (lane == 0) tg::mbar_arrive(&xch_free[quarter]);
       }
       const int row = tile * (kPair * kBM) + static_cast<int>(rank) * kBM + r;
       if (row < p.T) {
@@ -627,9 +665,9 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
     if (!encode_tmap_bf16(&tm_w, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return TG_ERR_CUDA;
   }
-  const SmemLayout L = score_smem_layout(p.item_n, ghp);
+  const SmemLayout L = score_smem_layout(p.item_n, ghp, rmsnorm);
   auto kernel = rmsnorm ? score_kernel_for<true>(ghp) : score_kernel_for<false>(ghp);
-  const int threads = rmsnorm ? kThreadsNorm : kThreads;
+  const int threads = kThreads;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
   // one wave of pairs: as many as fit at once (a pair sits in one GPC, so an odd SM is left out)
