@@ -47,10 +47,12 @@ constexpr uint32_t kTmemCols = 2 * kMaxItemN;
 constexpr int kMaxGateHeads = 16;
 constexpr int kPair = 2;  // CTAs of a cluster: the two halves (128 rows each) of a 256-row tile
 // Barrier region: full, empty and landed per stage (at most 7 stages), acc_full[2], acc_empty[2],
-// drain, rms_ready[2], rms_free[2], xch_full[4], xch_free[4]; then the tensor-memory slot and
-// three int32 flags.
-constexpr uint32_t kBarBytes = 320;
-static_assert((3 * 7 + 9 + 8) * 8 + 4 * 4 <= kBarBytes, "barrier region too small");
+// drain, rms_ready[2], rms_free[2], xch_full[4], xch_free[4], xq_full[4], xq_free[4]; then the
+// tensor-memory slot, three int32 flags and four reply words.
+constexpr uint32_t kBarBytes = 400;
+constexpr int kMaxQuadHeads = 8;  // padded gate heads up to which clusters of four are used
+constexpr uint32_t kSmemLimit = 232448;  // dynamic shared memory a CTA may opt into
+static_assert((3 * 7 + 9 + 8 + 8) * 8 + 4 * 4 + 4 * 4 <= kBarBytes, "barrier region too small");
 
 struct ScoreParams {
   int32_t T, d, d_g, n_items, item_n, n_tiles, KT;  // n_tiles: 256-row pair tiles
@@ -67,12 +69,13 @@ struct ScoreParams {
   int32_t *status;
   uint64_t wait_limit, drain_limit;
   int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
+  int32_t quad;      // clusters of four: the two pairs of a cluster take the two slices of a tile
 };
 
 __device__ const float g_zero_b1[kMaxDg] = {};  // b1 of a layer without a first-layer bias
 
 struct SmemLayout {
-  uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_rms, off_bar, total;
+  uint32_t a_bytes, b_bytes, off_b, off_w2, off_b1, off_rms, off_xq, off_bar, total;
 };
 
 // ghp: gate heads padded to 1, 2, 4, 8 or 16. More than one head keeps W2 as bf16 pairs
@@ -88,7 +91,10 @@ __host__ __device__ inline SmemLayout score_smem_layout(int item_n, int ghp, boo
   // fused RMSNorm: [2 tiles][128 rows] fp32 1 / rms; otherwise [ghp][128 rows] fp32, the
   // second-half epilogue warps' partial row sums handed to the first half
   L.off_rms = L.off_b1 + (ghp == 1 ? 0 : kMaxDg * 4);
-  L.off_bar = L.off_rms + (norm ? 2 * kBM * 4 : kBM * ghp * 4);
+  L.off_xq = L.off_rms + (norm ? 2 * kBM * 4 : kBM * ghp * 4);
+  // [ghp][128 rows] fp32: slice 1's partial sums (clusters of four, at most 8 heads: 16 heads
+  // leave no room for it beside six stages)
+  L.off_bar = L.off_xq + (ghp <= kMaxQuadHeads ? kBM * ghp * 4 : 0);
   L.total = L.off_bar + kBarBytes + 1024;  // barriers + slots, plus alignment slack
   return L;
 }
@@ -128,6 +134,14 @@ __device__ __forceinline__ void commit2_elect(uint32_t bar_cluster) {
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar_cluster)
       : "memory");
+}
+
+// A 4-byte store into the shared memory of another CTA of the cluster that, once it lands,
+// completes 4 bytes of the transaction count of the barrier at `bar_cluster` (in that CTA).
+__device__ __forceinline__ void st_async_b32(uint32_t addr_cluster, uint32_t v, uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr_cluster),
+               "r"(v), "r"(bar_cluster)
+               : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
@@ -194,7 +208,7 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&v)[NC], int hid, fl
 }
 
 template <bool NORM, int GHP>
-__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gate_score_kernel(const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -219,15 +233,21 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t *xch_full = landed + kStages;  // [4] per lane quarter: second-half partial sums written
   uint64_t *xch_free = xch_full + 4;      // [4] per lane quarter: the first half has read them
   float *s_xch = s_inv_rms;               // without the fused RMSNorm: [GHP][128 rows] partial sums
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xch_free + 4);
+  uint64_t *xq_full = xch_free + 4;       // [4] clusters of four: slice 1's partial sums landed here
+  uint64_t *xq_free = xq_full + 4;        // [4] slice 0's CTA has read them (its reply landed here)
+  float *s_xq = reinterpret_cast<float *>(smem + L.off_xq);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xq_free + 4);
   int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
   int32_t *n_issued = abort_flag + 1;
   int32_t *n_consumed = abort_flag + 2;
+  uint32_t *xq_word = reinterpret_cast<uint32_t *>(n_consumed + 1);  // [4] targets of the replies
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  uint32_t rank;
-  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  uint32_t crank;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  const uint32_t rank = crank & 1u;       // position in the CTA pair (peer CTAs differ in bit 0)
+  const uint32_t pb = crank & ~1u;        // cluster rank of the pair's leader
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
@@ -249,6 +269,8 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 4; ++i) {
       tg::mbar_init(&xch_full[i], 1);
       tg::mbar_init(&xch_free[i], 1);
+      tg::mbar_init(&xq_full[i], 1);
+      tg::mbar_init(&xq_free[i], 1);
     }
     *abort_flag = 0;
     *n_issued = 0;
@@ -286,14 +308,19 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
   bool tmem_ok;
   {
     uint32_t other;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(other) : "r"(cluster_addr(tmem_slot, rank ^ 1u)));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(other) : "r"(cluster_addr(tmem_slot, crank ^ 1u)));
     tmem_ok = other == tmem;
     if (!tmem_ok && threadIdx.x == 0) *vabort = 1;
   }
   // both halves of every stage land on the leader's full barrier
   const uint32_t stage_bytes = kPair * (L.a_bytes + L.b_bytes);
-  const int tile0 = blockIdx.x / kPair;
-  const int tile_stride = gridDim.x / kPair;
+  // a cluster is one pair, or (p.quad) two pairs that share each tile: pair crank / 2 takes slice
+  // crank / 2 of it, so a tile is one accumulator unit per pair instead of n_items
+  const int csize = p.quad ? 2 * kPair : kPair;
+  const int tile0 = blockIdx.x / csize;
+  const int tile_stride = gridDim.x / csize;
+  const int item_lo = p.quad ? static_cast<int>(crank >> 1) : 0;
+  const int item_hi = p.quad ? item_lo + 1 : p.n_items;
   const int half_n = p.item_n / kPair;  // W1 rows of a slice this CTA stages
 
   if (warp == 0) {
@@ -302,7 +329,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
       int kc = 0;
       bool ok = tmem_ok && !p.withhold;
       for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
-        for (int item = 0; item < p.n_items && ok; ++item) {
+        for (int item = item_lo; item < item_hi && ok; ++item) {
           for (int kt = 0; kt < p.KT; ++kt, ++kc) {
             const int st = kc % kStages;
             if (!tg::mbar_wait(&empty[st], ((kc / kStages) & 1) ^ 1u, vabort, p.wait_limit)) {
@@ -313,7 +340,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
             // this CTA's 128 rows of the 256-row h tile and its half of the W1 slice, completing on
             // the leader's barrier (the leader announces the bytes of both CTAs)
             if (leader) tg::mbar_arrive_expect_tx(&full[st], stage_bytes);
-            const uint32_t bar = cluster_addr(&full[st], 0);
+            const uint32_t bar = cluster_addr(&full[st], pb);
             tma_load_2d_to_leader(sA + st * L.a_bytes, &tm_h, bar, kt * kBK, tile * (kPair * kBM) + rank * kBM);
             tma_load_2d_to_leader(sB + st * L.b_bytes, &tm_w, bar, kt * kBK, item * p.item_n + rank * half_n);
             *n_issued = kc + 1;
@@ -335,7 +362,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
       int kc = 0, it = 0;
       bool ok = tmem_ok;
       for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
-        for (int item = 0; item < p.n_items && ok; ++item, ++it) {
+        for (int item = item_lo; item < item_hi && ok; ++item, ++it) {
           const int buf = it & 1;
           if (!__all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1u, vabort, p.wait_limit))) {
             ok = false;
@@ -356,22 +383,22 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
               mma2_bf16_ss_elect(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
             // the peer's norm warps may read their half once these MMAs have (a release arrival to
             // another CTA would cost this thread about 2,000 cycles; a commit costs it nothing)
-            if (NORM) commit2_elect(cluster_addr(&landed[st], 1));
+            if (NORM) commit2_elect(cluster_addr(&landed[st], pb | 1u));
             // the stage is free in both CTAs once these MMAs have read it
-            commit2_elect(cluster_addr(&empty[st], 0));
-            commit2_elect(cluster_addr(&empty[st], 1));
+            commit2_elect(cluster_addr(&empty[st], pb));
+            commit2_elect(cluster_addr(&empty[st], pb | 1u));
             if (lane == 0) *n_consumed = kc + 1;
           }
           if (ok) {
-            commit2_elect(cluster_addr(&acc_full[buf], 0));
-            commit2_elect(cluster_addr(&acc_full[buf], 1));
+            commit2_elect(cluster_addr(&acc_full[buf], pb));
+            commit2_elect(cluster_addr(&acc_full[buf], pb | 1u));
           }
         }
       }
       if (!ok) {
         *vabort = 1;
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
-        commit2_elect(cluster_addr(drain, 0));
+        commit2_elect(cluster_addr(drain, pb));
         volatile int32_t never = 0;
         tg::mbar_wait(drain, 0, &never, p.drain_limit);
       }
@@ -387,7 +414,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     const int g1 = (EW == 8 && half == 0) ? n_g / 2 : n_g;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     // accumulator units (tile, slice) this pair computes
-    const int n_units = tile0 < p.n_tiles ? ((p.n_tiles - 1 - tile0) / tile_stride + 1) * p.n_items : 0;
+    const int n_units = tile0 < p.n_tiles ? ((p.n_tiles - 1 - tile0) / tile_stride + 1) * (item_hi - item_lo) : 0;
     int it = 0, ti = 0;
     bool ok = tmem_ok;
     for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
@@ -403,7 +430,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         inv_rms = s_inv_rms[(ti & 1) * kBM + r];
       }
-      for (int item = 0; item < p.n_items; ++item, ++it) {
+      for (int item = item_lo; item < item_hi; ++item, ++it) {
         const int buf = it & 1;
         // tcgen05.ld is warp-collective: the whole warp takes the same branch
         ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&acc_full[buf], (it >> 1) & 1, vabort, p.wait_limit));
@@ -433,7 +460,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         // since a release arrival to another CTA holds its warp for about 2,000 cycles
         if (lane == 0) {
           if (leader) tg::mbar_arrive(&acc_empty[buf]);
-          else if (it + 2 < n_units) mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
+          else if (it + 2 < n_units) mbar_arrive_cluster(cluster_addr(&acc_empty[buf], pb));
         }
       }
       if (!ok) break;
@@ -464,6 +491,32 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
         for (int c = 0; c < GHP; ++c) acc[c] += s_xch[c * kBM + r];
         __syncwarp();
         if (lane == 0) tg::mbar_arrive(&xch_free[quarter]);
+      }
+      if (GHP <= kMaxQuadHeads && p.quad) {
+        // Clusters of four: slice 1's pair hands its partial sums to slice 0's CTA with the same
+        // rows (cluster rank crank - 2) as asynchronous remote stores that complete on that CTA's
+        // barrier (a release arrival to another CTA would hold this warp for ~2,000 cycles);
+        // slice 0 adds them after its own (slice order) and writes the row's results, then
+        // replies with one word so the buffer may be refilled.
+        if (crank >= 2) {
+          if (ti > 0) {
+            if (lane == 0) tg::mbar_arrive_expect_tx(&xq_free[quarter], 4u);
+            ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&xq_free[quarter], (ti - 1) & 1, vabort, p.wait_limit));
+            if (!ok) break;
+          }
+          const uint32_t bar = cluster_addr(&xq_full[quarter], crank - 2);
+#pragma unroll
+          for (int c = 0; c < GHP; ++c) st_async_b32(cluster_addr(&s_xq[c * kBM + r], crank - 2), __float_as_uint(acc[c]), bar);
+          continue;
+        }
+        if (lane == 0) tg::mbar_arrive_expect_tx(&xq_full[quarter], 32u * GHP * 4u);
+        ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(&xq_full[quarter], ti & 1, vabort, p.wait_limit));
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < GHP; ++c) acc[c] += s_xq[c * kBM + r];
+        __syncwarp();
+        if (lane == 0 && tile + tile_stride < p.n_tiles)
+          st_async_b32(cluster_addr(&xq_word[quarter], crank + 2), 1u, cluster_addr(&xq_free[quarter], crank + 2));
       }
       const int row = tile * (kPair * kBM) + static_cast<int>(rank) * kBM + r;
       if (row < p.T) {
@@ -499,7 +552,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = tmem_ok;
     for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride, ++ti) {
       float sq = 0.0f;
-      for (int item = 0; item < p.n_items && ok; ++item) {
+      for (int item = item_lo; item < item_hi && ok; ++item) {
         for (int kt = 0; kt < p.KT; ++kt, ++kc) {
           const int st = kc % kStages;
           // the peer's stages complete on the leader's barrier; its norm warps learn that a stage
@@ -507,7 +560,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(leader ? &full[st] : &landed[st], (kc / kStages) & 1, vabort,
                                                      p.wait_limit));
           if (!ok) break;
-          if (item == 0) {  // every slice re-reads the same h tile; the first pass suffices
+          if (item == item_lo) {  // every slice re-reads the same h tile; the first pass suffices
             const uint4 *row_base = reinterpret_cast<const uint4 *>(sA + st * L.a_bytes + r * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -524,7 +577,7 @@ __global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) tg::mbar_arrive(&empty[st]);
         }
-        if (ok && item == 0) {
+        if (ok && item == item_lo) {
           ok = __all_sync(0xFFFFFFFFu,
                           tg::mbar_wait(&rms_free[ti & 1], ((ti >> 1) & 1) ^ 1u, vabort, p.wait_limit));
           if (!ok) break;
@@ -566,14 +619,15 @@ namespace tg_host {
 
 namespace {
 
-// CTA pairs that are resident at once for this kernel and shared-memory size (cached per
-// device, kernel and size; at least one).
-cudaError_t resident_pairs(const void *kernel, int threads, size_t smem, int *pairs) {
+// Clusters of `csize` CTAs that are resident at once for this kernel and shared-memory size
+// (cached per device, kernel, size and cluster size; at least one).
+cudaError_t resident_clusters(const void *kernel, int threads, size_t smem, int csize, int *clusters) {
   struct Entry {
     int dev;
     const void *kernel;
     size_t smem;
-    int pairs;
+    int csize;
+    int clusters;
   };
   static std::mutex mu;
   static std::vector<Entry> cache;
@@ -582,17 +636,17 @@ cudaError_t resident_pairs(const void *kernel, int threads, size_t smem, int *pa
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   for (const Entry &c : cache)
-    if (c.dev == dev && c.kernel == kernel && c.smem == smem) {
-      *pairs = c.pairs;
+    if (c.dev == dev && c.kernel == kernel && c.smem == smem && c.csize == csize) {
+      *clusters = c.clusters;
       return cudaSuccess;
     }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kPair * num_sms());
+  cfg.gridDim = dim3(csize * num_sms());
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -601,9 +655,30 @@ cudaError_t resident_pairs(const void *kernel, int threads, size_t smem, int *pa
   e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) n = 1;
-  cache.push_back({dev, kernel, smem, n});
-  *pairs = n;
+  cache.push_back({dev, kernel, smem, csize, n});
+  *clusters = n;
   return cudaSuccess;
+}
+
+// Launch with the cluster size given at run time and programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_clusters(void (*kernel)(KArgs...), int clusters, int csize, int threads, size_t smem,
+                            cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * csize);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <bool NORM>
@@ -649,6 +724,7 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   p.wait_limit = wait_limit_ns();
   p.drain_limit = drain_limit_ns();
   p.withhold = (withhold_mask() & TG_WITHHOLD_GATE_SCORE) != 0;
+  p.quad = 0;
 
   CUtensorMap tm_h, tm_w;
   {
@@ -666,16 +742,33 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
       return TG_ERR_CUDA;
   }
   const SmemLayout L = score_smem_layout(p.item_n, ghp, rmsnorm);
+  if (L.total > kSmemLimit) return TG_ERR_UNSUPPORTED;
   auto kernel = rmsnorm ? score_kernel_for<true>(ghp) : score_kernel_for<false>(ghp);
   const int threads = kThreads;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return record_cuda(e);
-  // one wave of pairs: as many as fit at once (a pair sits in one GPC, so an odd SM is left out)
+  // One wave of clusters: as many as fit at once (a cluster sits in one GPC). Pairs walk the
+  // tiles with both slices each; clusters of four, where the two pairs take the two slices of a
+  // tile side by side, when that takes fewer slice-rounds (few tiles for many SMs).
   int pairs = 0;
-  e = resident_pairs(reinterpret_cast<const void *>(kernel), threads, L.total, &pairs);
+  e = resident_clusters(reinterpret_cast<const void *>(kernel), threads, L.total, kPair, &pairs);
   if (e != cudaSuccess) return record_cuda(e);
-  if (pairs > p.n_tiles) pairs = p.n_tiles;
-  return record_cuda(launch_pdl(kernel, dim3(kPair * pairs), dim3(threads), L.total, stream, tm_h, tm_w, p));
+  p.quad = 0;
+  int csize = kPair, clusters = pairs;
+  if (p.n_items == 2 && ghp <= kMaxQuadHeads) {
+    int quads = 0;
+    e = resident_clusters(reinterpret_cast<const void *>(kernel), threads, L.total, 2 * kPair, &quads);
+    if (e != cudaSuccess) return record_cuda(e);
+    const int rounds_pair = 2 * ((p.n_tiles + pairs - 1) / pairs);
+    const int rounds_quad = (p.n_tiles + quads - 1) / quads;
+    if (rounds_quad < rounds_pair) {
+      p.quad = 1;
+      csize = 2 * kPair;
+      clusters = quads;
+    }
+  }
+  if (clusters > p.n_tiles) clusters = p.n_tiles;
+  return record_cuda(launch_clusters(kernel, clusters, csize, threads, L.total, stream, tm_h, tm_w, p));
 }
 
 // ---------------------------------------------------------------------------
