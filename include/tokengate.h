@@ -427,10 +427,17 @@ TG_API tg_status tg_set_wait_limit_ns(uint64_t limit_ns);
  *   the kernel sets TG_DEV_TIMEOUT, frees its tensor memory and returns, and the CUDA context
  *   stays usable. Nothing faults or hangs. Bits: TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION,
  *   TG_WITHHOLD_BACKWARD (the dK/dV and dQ passes of tg_gated_attention_bwd);
+ *   TG_WITHHOLD_GATE_SCORE_PEER (only the gate-score CTAs of odd cluster rank withhold theirs,
+ *   so every CTA pair loses one half of each stage while the other half lands);
  *   0 (the default) clears them. Any other bit is TG_ERR_INVALID_ARG. Process-wide; takes
  *   effect for later launches.
  */
-enum { TG_WITHHOLD_GATE_SCORE = 1 << 0, TG_WITHHOLD_ATTENTION = 1 << 1, TG_WITHHOLD_BACKWARD = 1 << 2 };
+enum {
+  TG_WITHHOLD_GATE_SCORE = 1 << 0,
+  TG_WITHHOLD_ATTENTION = 1 << 1,
+  TG_WITHHOLD_BACKWARD = 1 << 2,
+  TG_WITHHOLD_GATE_SCORE_PEER = 1 << 3
+};
 TG_API tg_status tg_set_test_withhold(int32_t mask);
 
 #ifdef __cplusplus

@@ -353,7 +353,7 @@ def set_wait_limit_ns(ns: int):
     _check("tg_set_wait_limit_ns", load().tg_set_wait_limit_ns(int(ns)))
 
 
-TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION, TG_WITHHOLD_BACKWARD = 1, 2, 4
+TG_WITHHOLD_GATE_SCORE, TG_WITHHOLD_ATTENTION, TG_WITHHOLD_BACKWARD, TG_WITHHOLD_GATE_SCORE_PEER = 1, 2, 4, 8
 
 
 def set_test_withhold(mask: int):

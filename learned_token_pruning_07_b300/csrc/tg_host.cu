@@ -106,7 +106,8 @@ tg_status tg_set_wait_limit_ns(uint64_t limit_ns) {
 }
 
 tg_status tg_set_test_withhold(int32_t mask) {
-  if (mask & ~(TG_WITHHOLD_GATE_SCORE | TG_WITHHOLD_ATTENTION | TG_WITHHOLD_BACKWARD)) return TG_ERR_INVALID_ARG;
+  if (mask & ~(TG_WITHHOLD_GATE_SCORE | TG_WITHHOLD_ATTENTION | TG_WITHHOLD_BACKWARD | TG_WITHHOLD_GATE_SCORE_PEER))
+    return TG_ERR_INVALID_ARG;
   g_withhold.store(mask, std::memory_order_relaxed);
   return TG_OK;
 }

@@ -68,7 +68,7 @@ struct ScoreParams {
   float *s_sel;  // H_g > 1: [T] uniform head aggregation (the row mean) that top-K ranks
   int32_t *status;
   uint64_t wait_limit, drain_limit;
-  int32_t withhold;  // test hook: issue no loads, so the consumers' waits run out
+  int32_t withhold;  // test hook: 1: no CTA issues its loads; 2: CTAs of odd cluster rank issue none
   int32_t quad;      // clusters of four: the two pairs of a cluster take the two slices of a tile
 };
 
@@ -142,6 +142,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr_cluster, uint32_t v, 
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr_cluster),
                "r"(v), "r"(bar_cluster)
                : "memory");
+}
+
+// Raise the abort flag in every CTA of the cluster (a plain store into each one's shared
+// memory), so that all of them stop issuing and leave their waits together.
+__device__ __forceinline__ void raise_abort(int32_t *abort_flag, uint32_t crank, int csize) {
+  *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
+  for (int r = 0; r < csize; ++r)
+    if (static_cast<uint32_t>(r) != crank)
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(abort_flag, static_cast<uint32_t>(r))), "r"(1)
+                   : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
@@ -327,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---- TMA producer: stage = h tile [128 x 64] + W1 slice [item_n x 64] ----
       int kc = 0;
-      bool ok = tmem_ok && !p.withhold;
+      bool ok = tmem_ok && !(p.withhold == 1 || (p.withhold == 2 && (crank & 1u)));
       for (int tile = tile0; tile < p.n_tiles && ok; tile += tile_stride) {
         for (int item = item_lo; item < item_hi && ok; ++item) {
           for (int kt = 0; kt < p.KT; ++kt, ++kc) {
             const int st = kc % kStages;
             if (!tg::mbar_wait(&empty[st], ((kc / kStages) & 1) ^ 1u, vabort, p.wait_limit)) {
-              *vabort = 1;
+              raise_abort(abort_flag, crank, csize);
               ok = false;
               break;
             }
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tail: the leader's last commits to this CTA's stage barriers have landed before it exits
       for (int k = kc - kStages < 0 ? 0 : kc - kStages; ok && k < kc; ++k)
         ok = tg::mbar_wait(&empty[k % kStages], (k / kStages) & 1, vabort, p.wait_limit);
-      if (!ok) *vabort = 1;
+      if (!ok) raise_abort(abort_flag, crank, csize);
     }
   } else if (warp == 1) {
     if (leader) {
@@ -396,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        *vabort = 1;
+        raise_abort(abort_flag, crank, csize);
         // drain: wait for the MMAs already issued before the tiles and TMEM go away
         commit2_elect(cluster_addr(drain, pb));
         volatile int32_t never = 0;
@@ -543,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok) *vabort = 1;
+    if (!ok) raise_abort(abort_flag, crank, csize);
   } else if (NORM) {
     // ---- norm warps: sum of squares of each row of the tile as its h stages stream past ----
     // Row r of a 128-byte-swizzled stage holds its eight 16-byte chunks at positions c ^ (r % 8).
@@ -587,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok) *vabort = 1;
+    if (!ok) raise_abort(abort_flag, crank, csize);
   }
 
   tg::tc_fence_before();
@@ -597,10 +607,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg::report(p.status, TG_DEV_TIMEOUT);
       // wait (bounded) for TMA copies that were issued but never consumed; the copies of both
       // CTAs complete on the leader's barriers
+      // (one budget for all of them: when a peer withheld its half, these phases never complete)
       volatile int32_t never = 0;
-      if (leader)
-        for (int i = *n_consumed; i < *n_issued; ++i)
-          tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.drain_limit);
+      if (leader) {
+        const uint64_t t0 = tg::globaltimer_ns();
+        for (int i = *n_consumed; i < *n_issued; ++i) {
+          const uint64_t spent = tg::globaltimer_ns() - t0;
+          if (spent >= p.drain_limit) break;
+          tg::mbar_wait(&full[i % kStages], (i / kStages) & 1, &never, p.drain_limit - spent);
+        }
+      }
     }
     __syncthreads();
   }
@@ -723,7 +739,7 @@ tg_status launch_gate_score(const uint16_t *h, int32_t T, int32_t d, const uint8
   p.status = status;
   p.wait_limit = wait_limit_ns();
   p.drain_limit = drain_limit_ns();
-  p.withhold = (withhold_mask() & TG_WITHHOLD_GATE_SCORE) != 0;
+  p.withhold = (withhold_mask() & TG_WITHHOLD_GATE_SCORE) ? 1 : (withhold_mask() & TG_WITHHOLD_GATE_SCORE_PEER) ? 2 : 0;
   p.quad = 0;
 
   CUtensorMap tm_h, tm_w;

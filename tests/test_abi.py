@@ -96,9 +96,11 @@ def test_wait_limit_setter(lib):
 
 
 def test_test_withhold_hook_validates_its_mask(lib):
-    all_bits = binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION | binding.TG_WITHHOLD_BACKWARD
+    all_bits = (binding.TG_WITHHOLD_GATE_SCORE | binding.TG_WITHHOLD_ATTENTION | binding.TG_WITHHOLD_BACKWARD
+                | binding.TG_WITHHOLD_GATE_SCORE_PEER)
+    assert all_bits == 15
     assert lib.tg_set_test_withhold(all_bits) == binding.TG_OK
-    assert lib.tg_set_test_withhold(8) == binding.TG_ERR_INVALID_ARG
+    assert lib.tg_set_test_withhold(16) == binding.TG_ERR_INVALID_ARG
     assert lib.tg_set_test_withhold(0) == binding.TG_OK
 
 

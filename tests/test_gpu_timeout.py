@@ -58,6 +58,25 @@ def test_gate_score_wait_runs_out_then_recovers(withheld):
     np.testing.assert_allclose(host(g), ref_g, rtol=0, atol=G_ATOL)
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen3_1p7b_8k"])
+def test_gate_score_one_cta_of_each_pair_withholds(withheld, name):
+    # Only the CTAs of odd cluster rank issue no loads: every stage of the leader's barrier
+    # misses one half, the MMAs never start, and the abort raised by the CTA that gives up first
+    # reaches every CTA of the cluster (pairs at the tiny size, clusters of four at 8K). The
+    # drain is bounded in total, and the next call is correct.
+    wl = I.WORKLOADS[name]
+    withheld(tg.TG_WITHHOLD_GATE_SCORE_PEER)
+    _, _, st = _score(wl)
+    assert tg.read_device_status(st) & tg.TG_DEV_TIMEOUT
+    tg.set_test_withhold(0)
+    tg.set_wait_limit_ns(0)
+    gi, g, st = _score(wl)
+    assert tg.read_device_status(st) == 0
+    _, ref_g = O.gate_score(I.bf16_bits_to_f64(gi["h"]), I.bf16_bits_to_f64(gi["W1"]),
+                            I.bf16_bits_to_f64(gi["w2"]), gi["instr_mask"])
+    np.testing.assert_allclose(host(g), ref_g, rtol=0, atol=G_ATOL)
+
+
 def _attention(wl, M):
     at = I.make_attention_inputs(wl, M)
     cu = I.cu_seqlens_of([M])
