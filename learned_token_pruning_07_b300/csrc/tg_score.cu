@@ -2,28 +2,36 @@
 //
 //   u = W1 h_j (+ b1),  s_j = w2 . SiLU(u) (+ b2),  g_j = sigmoid(s_j)  (g = 1 on non-prunable rows)
 //
-// Persistent kernel on CTA pairs (clusters of two, one CTA per SM): a pair walks 256-row tiles
-// of h (pair tile = pair index + k * pairs). The d_g-wide hidden layer of a tile is computed as
-// n_items column slices of at most 256 (two slices of 256 at d_g = 512). Each slice is one work
-// item: a d-reduction u_slice = h_tile W1_slice^T issued as 2-SM tensor-core MMAs
+// Persistent kernel on CTA pairs (one CTA per SM): a pair walks 256-row tiles of h (pair tile =
+// pair index + k * pairs). The d_g-wide hidden layer of a tile is computed as n_items column
+// slices of at most 256 (two slices of 256 at d_g = 512). A slice is one accumulator unit: a
+// d-reduction u_slice = h_tile W1_slice^T issued as 2-SM tensor-core MMAs
 // (tcgen05.mma.cta_group::2 kind::f16, M = 256): CTA r of the pair stages its own 128 rows of the
 // h tile and its half (rows r * item_n / 2 ..) of the W1 slice, and the tensor cores of the two
 // SMs share the W1 halves, so each SM takes in 32 KB per K-stage of 64 instead of 48 KB. (With
 // every SM loading at once, shared memory fills at about 60 B/clk per SM on this part, under the
 // 94 B/clk that one-CTA 128 x 256 tiles would need to keep their MMAs busy.) The accumulator of
 // a CTA's 128 rows is in its own tensor memory, in one of two 256-column buffers: the epilogue of
-// item i (SiLU, the w2 dot, and at a tile's last slice the sigmoid) runs while the tensor cores
-// already work on item i+1 in the other buffer. A row's partial w2 dots of its slices are summed
-// in registers by the same thread, in slice order, so s is deterministic and no scratch memory
-// is needed.
+// a unit (SiLU, the w2 dot, and at a tile's last slice the sigmoid) runs while the tensor cores
+// already work on the next unit in the other buffer.
 //
-// Warp roles: warp 0 lane 0 of each CTA issues that CTA's TMA loads, which complete on the
-// leader's (rank 0's) stage barrier; warp 1 owns tensor memory (allocated for the pair), and in
+// With two slices and few tiles for many SMs, the launch uses clusters of four instead: the two
+// pairs of a cluster take the two slices of the same tile side by side, and slice 1's CTA hands
+// its rows' partial w2 dots to slice 0's CTA with asynchronous remote stores.
+//
+// Every partial w2 dot of a row is added in a fixed order (column halves, then slices), so s
+// is deterministic, and no global scratch memory is needed.
+//
+// Warp roles (320 threads): warp 0 lane 0 of each CTA issues that CTA's TMA loads, which complete
+// on the pair leader's stage barrier; warp 1 owns tensor memory (allocated for the pair), and in
 // the leader issues the MMAs (the warp runs converged and one elected lane issues) and commits
-// their completion to the barriers of both CTAs; warps 2-5 run the epilogue (warp w reads
-// tensor-memory lanes 32*(w%4) .. +31, one row per thread) and report a drained accumulator to
-// the leader. Every wait is bounded (see tg_set_wait_limit_ns); a wait that gives up sets
-// TG_DEV_TIMEOUT, drains the copies and MMAs in flight, frees tensor memory and returns.
+// their completion to the barriers of both CTAs; warps 2-9 run the epilogue, two per
+// tensor-memory lane quarter (warp w reads lanes 32*(w%4) .. +31, one row per thread, half of
+// the columns each), and report a drained accumulator to the leader. With the fused RMSNorm,
+// warps 2-5 run the epilogue over all columns and warps 6-9 sum each row's squares. Every wait
+// is bounded (see tg_set_wait_limit_ns); a wait that gives up raises the abort flag in every CTA
+// of the cluster and sets TG_DEV_TIMEOUT; the CTAs drain the copies and MMAs in flight, free
+// tensor memory and return.
 #include <mutex>
 #include <vector>
 
