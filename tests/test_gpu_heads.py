@@ -101,6 +101,15 @@ def test_score_heads_slices_of_an_odd_multiple_of_16():
     _score_heads(wl, 16, rmsnorm=True)
 
 
+def test_score_heads_clusters_of_four_several_tiles():
+    # 80 pair tiles with 8 gate heads: clusters of four, several tiles each (see test_gpu_score)
+    wl = I.with_changes(I.WORKLOADS["sweep_32k"], doc_lens=(20224,), instr_lens=(256,))
+    rng = np.random.default_rng(31)
+    rows = np.unique(np.concatenate([np.arange(0, 300), np.arange(wl.T_total - 300, wl.T_total),
+                                     rng.integers(0, wl.T_total, 1500)]))
+    _score_heads(wl, 8, rows=rows)
+
+
 def test_score_heads_qwen3_gate_layer_8k():
     _score_heads(I.WORKLOADS["qwen3_1p7b_8k"], 16)
 

@@ -137,6 +137,16 @@ def test_score_rmsnorm_slices_of_an_odd_multiple_of_16():
     _rmsnorm_case(I.with_changes(I.WORKLOADS["tiny"], doc_lens=(700,), instr_lens=(9,), d=256, d_g=288))
 
 
+def test_score_rmsnorm_clusters_of_four_several_tiles():
+    # 20,480 rows = 80 pair tiles: the launch takes clusters of four (fewer slice-rounds than pairs),
+    # each with several tiles, so slice 1's partial sums are handed over again after the reply
+    wl = I.with_changes(I.WORKLOADS["sweep_32k"], doc_lens=(20224,), instr_lens=(256,))
+    rng = np.random.default_rng(29)
+    rows = np.unique(np.concatenate([np.arange(0, 300), np.arange(wl.T_total - 300, wl.T_total),
+                                     rng.integers(0, wl.T_total, 1500)]))
+    _rmsnorm_case(wl, rows=rows)
+
+
 def test_score_rmsnorm_qwen3_gate_layer_8k():
     _rmsnorm_case(I.WORKLOADS["qwen3_1p7b_8k"])
 
