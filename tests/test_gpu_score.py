@@ -157,3 +157,32 @@ def test_score_rmsnorm_full_size_sweep_sampled_rows():
     rows = np.unique(np.concatenate([np.arange(0, 200), np.arange(wl.T_total - 200, wl.T_total),
                                      rng.integers(0, wl.T_total, 1500)]))
     _rmsnorm_case(wl, rows=rows)
+
+
+@pytest.mark.parametrize("name,doc", [("sweep_32k", None), ("qwen3_1p7b_8k", None), ("sweep_32k", 20224)])
+def test_score_is_bit_identical_across_runs(name, doc):
+    # Pairs at 32K, clusters of four at 8K and 20K: every partial w2 dot is added in a fixed
+    # order (column halves, then slices), so two runs give the same bits, with and without the
+    # fused RMSNorm and with eight gate heads
+    wl = I.WORKLOADS[name] if doc is None else I.with_changes(I.WORKLOADS[name], doc_lens=(doc,), instr_lens=(256,))
+    gi = I.make_gate_inputs(wl)
+    T = wl.T_total
+    h, W1, w2, mask = dev(gi["h"]), dev(gi["W1"]), dev(gi["w2"]), dev(gi["instr_mask"])
+    W2 = dev(I.make_gate_head_weights(wl, 8)["W2"])
+
+    def run():
+        s = torch.empty(T, dtype=torch.float32, device="cuda")
+        g = torch.empty(T, dtype=torch.float32, device="cuda")
+        tg.gate_score(h, W1, w2, s, g, instr_mask=mask)
+        sn = torch.empty(T, dtype=torch.float32, device="cuda")
+        tg.gate_score_rmsnorm(h, W1, w2, sn, instr_mask=mask)
+        sh = torch.empty(T, 8, dtype=torch.float32, device="cuda")
+        sel = torch.empty(T, dtype=torch.float32, device="cuda")
+        tg.gate_score_heads(h, W1, W2, sh, sel, instr_mask=mask)
+        torch.cuda.synchronize()
+        return [host(x).view(np.uint32).copy() for x in (s, g, sn, sh, sel)]
+
+    first, second = run(), run()
+    for a, b in zip(first, second):
+        assert np.array_equal(a, b)
+
