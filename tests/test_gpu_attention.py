@@ -128,6 +128,27 @@ def test_attention_sweep_k16384_sampled_rows():
     _assert_close(*_run(wl, [M], rows=rows))
 
 
+def test_attention_back_to_back_launches_never_time_out():
+    # Many launches queued without a host sync, at a length where every CTA walks up to 260 key
+    # tiles: the pipeline barriers must hold their phases whatever the relative speed of the
+    # softmax and MMA warps (a phase overrun shows as a timeout in the status word)
+    wl = I.WORKLOADS["sweep_32k"]
+    M = 16384 + 256
+    at = I.make_attention_inputs(wl, M, tag_extra=3)
+    Qd, Kd, Vd, gd, cud = dev(at["Q"]), dev(at["K"]), dev(at["V"]), dev(at["g"]), dev(I.cu_seqlens_of([M]))
+    st = status_word()
+    outs = [torch.empty((M, wl.H_q, wl.d_h), dtype=torch.int16, device="cuda") for _ in range(2)]
+    tg.set_wait_limit_ns(200_000_000)
+    try:
+        for i in range(24):
+            tg.gated_attention(Qd, Kd, Vd, cud, at["tau"], at["beta"], outs[i % 2], max_seqlen=M, g=gd, status=st)
+        torch.cuda.synchronize()
+    finally:
+        tg.set_wait_limit_ns(0)
+    assert int(host(st)[0]) == 0
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_attention_ragged_batch_sampled_rows():
     wl = I.WORKLOADS["ragged_b8"]
     lens = [min(2048, d) + n for d, n in zip(wl.doc_lens, wl.instr_lens)]
