@@ -88,6 +88,16 @@ def test_select_full_size(name):
         _check_select(s, mask, cu, K)
 
 
+@pytest.mark.parametrize("doc_lens,instr_lens", [((60000, 150), (300, 50)), ((60000,), (300,))])
+def test_select_long_sequences_with_ties(doc_lens, instr_lens):
+    # a 60K sequence (7,500 keys per CTA of its cluster), alone and next to a short one;
+    # quantised scores keep ties at the threshold, and K = 40000 keeps most of the long one
+    wl = I.with_changes(I.WORKLOADS["ragged_b8"], doc_lens=doc_lens, instr_lens=instr_lens, score_levels=256)
+    s = I.make_scores(wl)
+    for K in (1, 777, 40000):
+        _check_select(s, I.make_instr_mask(wl), I.cu_seqlens_of(wl.seq_lens), K)
+
+
 def test_select_capacity_overflow_is_reported_and_bounded():
     wl = I.WORKLOADS["tiny"]
     s = I.make_scores(wl)
