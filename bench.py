@@ -295,16 +295,20 @@ class GraphStep:
     up on the device timeline. Two graphs: `whole` records events only around the step, so
     each kernel's launch may overlap the previous kernel's tail (programmatic dependent
     launch) -- this one gives the step time; `staged` records an event between every two
-    kernels and gives the per-kernel breakdown."""
+    kernels and gives the per-kernel breakdown. A third, `paired`, has no event between the
+    selection and the gather, so the pair is timed as the fused call runs it (the gather's
+    launch overlapping the selection's tail)."""
 
     def __init__(self, path, torch):
         self.torch = torch
         self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
         self.ew = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        self.ep = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         path.step()                      # first launch sets kernel attributes outside capture
         torch.cuda.synchronize()
         self.staged = self._capture(path, self.ev)
         self.whole = self._capture(path, [self.ew[0], None, None, None, self.ew[1]])
+        self.paired = self._capture(path, [self.ep[0], self.ep[1], None, self.ep[2], self.ep[3]])
         self.graph = self.whole
 
     def _capture(self, path, ev):
@@ -322,6 +326,9 @@ class GraphStep:
 
     def replay(self, staged=False):
         (self.staged if staged else self.whole).replay()
+
+    def pair_time(self):
+        return self.ep[1].elapsed_time(self.ep[2])
 
     def step_time(self):
         return self.ew[0].elapsed_time(self.ew[1])
@@ -361,6 +368,17 @@ def time_stages(gstep, steps, torch, flush):
         torch.cuda.synchronize()
         per_stage.append(gstep.times())
     return np.array(per_stage)
+
+
+def time_pairs(gstep, steps, torch, flush):
+    """Selection + gather with no event between them (the `paired` graph), L2 flushed between steps."""
+    out = []
+    for _ in range(steps):
+        flush()
+        gstep.paired.replay()
+        torch.cuda.synchronize()
+        out.append(gstep.pair_time())
+    return np.array(out)
 
 
 def time_device_steps(gstep, steps, torch, flush):
@@ -764,13 +782,19 @@ def stage_summary(work, per_stage, peaks):
     return stages
 
 
-def select_gather_summary(work, stages, peaks):
+def select_gather_summary(work, stages, peaks, paired_ms=None):
     """Selection and gather together against HBM: selection alone moves too few bytes to mean
-    anything against HBM bandwidth."""
+    anything against HBM bandwidth. `us` / `frac` add the two staged kernel times; `paired_*`
+    time the pair back to back with no event between them, as the fused call runs it."""
     us = stages["topk_select"]["us"] + stages["gather_kept"]["us"]
     by = work["topk_select"]["bytes"] + work["gather_kept"]["bytes"]
-    return {"us": us, "bytes": by, "achieved_gbs": by / (us * 1e-6) / 1e9,
-            "frac": by / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    out = {"us": us, "bytes": by, "achieved_gbs": by / (us * 1e-6) / 1e9,
+           "frac": by / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    if paired_ms is not None:
+        pu = float(paired_ms) * 1000.0
+        out.update({"paired_us": pu, "paired_achieved_gbs": by / (pu * 1e-6) / 1e9,
+                    "paired_frac": by / (pu * 1e-6) / 1e9 / peaks["hbm_gbs"]})
+    return out
 
 
 def other_configs(torch, flush, steps, peaks, rank, with_oracle=True):
@@ -786,13 +810,14 @@ def other_configs(torch, flush, steps, peaks, rank, with_oracle=True):
         g = GraphStep(p, torch)
         warm(g, 3, torch, flush)
         ps, pst = time_device_steps(g, max(5, min(steps, 30)), torch, flush)
+        pair = time_pairs(g, max(5, min(steps, 30)), torch, flush)
         assert p.tg.read_device_status(p.status) == 0, "device reported an error"
         work = stage_work(wl, wl.K, p.kept_lens)
         st = stage_summary(work, pst, peaks)
         ms = float(ps.mean())
         entry = {"workload": workload_label(base, wl.K), "K": wl.K, "T_total": wl.T_total, "M_kept": p.M,
                  "value": wl.T_total / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "stages": st,
-                 "select_plus_gather": select_gather_summary(work, st, peaks),
+                 "select_plus_gather": select_gather_summary(work, st, peaks, float(pair.mean())),
                  "selection_scores": ("synthetic 256-level quantised buffer" if wl.score_levels
                                       else "the step's own gate scores")}
         del g, p
@@ -891,6 +916,7 @@ def run_gpu(args, rank, world, local):
         torch.distributed.barrier()
     wall = time.perf_counter() - t_wall0
     per_stage = time_stages(gstep, args.steps, torch, flush)
+    per_pair = time_pairs(gstep, args.steps, torch, flush)
     # keep the GPU busy a little longer so the sampler sees the clocks under this load
     t_end = time.perf_counter() + max(0.0, 1.0 - wall)
     while time.perf_counter() < t_end:
@@ -961,7 +987,7 @@ def run_gpu(args, rank, world, local):
             "config": config_dict(base, K, world),
             "roofline": roof,
             "stages": stages,
-            "select_plus_gather": select_gather_summary(work, stages, peaks),
+            "select_plus_gather": select_gather_summary(work, stages, peaks, float(per_pair.mean())),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": path.h2d_bytes(), "d2h_bytes_per_step": path.d2h_bytes(),
