@@ -569,20 +569,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[static_cast<size_t>(seq_start + row) * p.H_q + h] =
               l > 0.0f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
-        uint16_t *orow = p.O + (static_cast<size_t>(seq_start + row) * p.H_q + h) * D;
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
-          tg::tmem_ld_wait();
-          if (row < seq_len) {
+        // A thread's row sits H_q * D elements from the next one, so storing rows straight from
+        // registers would touch a separate sector per lane. The rows go through this head's Q
+        // buffer instead (its S MMAs have all completed, o_final being committed after them),
+        // 16-byte chunks XOR-swizzled by row so both sides spread over the banks; then each warp
+        // writes its own 32 rows with kChunks lanes per row. (A split launch keeps the direct
+        // stores: measured, the staging slowed its key loop more than it saved.)
+        if constexpr (SPLIT) {
+          uint16_t *orow = p.O + (static_cast<size_t>(seq_start + row) * p.H_q + h) * D;
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
+            tg::tmem_ld_wait();
+            if (row < seq_len) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = tg::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+          }
+        } else {
+          constexpr int kChunks = D / 8;  // 16-byte chunks per row
+          uint4 *stg = reinterpret_cast<uint4 *>(sQ + t * C::kTileBytes);
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tg::tmem_ld_32x32b_x32(lane_addr + colO + c0, o);
+            tg::tmem_ld_wait();
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              w[i] = tg::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                     __uint_as_float(o[2 * i + 1]) * inv_l);
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+              w[i] = tg::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              stg[r * kChunks + ((c0 / 8 + i) ^ (r & (kChunks - 1)))] =
+                  make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+          __syncwarp();
+          constexpr int kRowsPerStep = 32 / kChunks;
+          const int cl = lane % kChunks;
+#pragma unroll 8
+          for (int rr = 0; rr < 32; rr += kRowsPerStep) {
+            const int rt = wq * 32 + rr + lane / kChunks;  // row within the tile
+            const uint4 v = stg[rt * kChunks + (cl ^ (rt & (kChunks - 1)))];
+            if (q0 + rt < seq_len)
+              reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(seq_start + q0 + rt) * p.H_q + h) * D)[cl] = v;
           }
         }
       }
