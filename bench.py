@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -118,13 +119,21 @@ def load_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without its comments and blank lines, so a comment-only edit keeps the hash."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(name: str) -> str:
+    """Hash of the code (comments stripped) of a kernel's source file and the common header."""
     files = {"gate_score": "tg_score.cu", "topk_select": "tg_select.cu", "gather_kept": "tg_gather.cu",
              "gated_attention": "tg_attention.cu"}
     h = hashlib.sha256()
     for f in (files[name], "tg_common.cuh"):
-        with open(os.path.join(ROOT, "learned_token_pruning_07_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "learned_token_pruning_07_b300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
