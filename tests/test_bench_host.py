@@ -64,6 +64,15 @@ def test_each_kernel_has_its_own_source_hash():
     assert len(set(hashes.values())) == 4 and all(len(v) == 16 for v in hashes.values())
 
 
+def test_source_hash_ignores_comments_but_not_code():
+    src = 'int a = 1; // one\n/* a block\n   comment */\nint b = a + 2;\n\n  // indented note\n'
+    same = 'int a = 1;\nint b = a + 2; /* trailing */\n'
+    changed = 'int a = 1;\nint b = a + 3;\n'
+    assert bench.strip_comments(src) == bench.strip_comments(same)
+    assert bench.strip_comments(src) != bench.strip_comments(changed)
+    assert "//" not in bench.strip_comments(src) and "/*" not in bench.strip_comments(src)
+
+
 def test_peaks_come_from_the_measured_file_when_present():
     p = bench.load_peaks()
     path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
