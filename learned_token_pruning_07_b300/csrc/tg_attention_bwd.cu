@@ -520,19 +520,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(acc_final, 0, vabort, p.wait_limit));
     if (ok) {
       tg::tc_fence_after();
-      float *out = (hh == 0 ? p.dV : p.dK) + (static_cast<size_t>(seq_start + kj) * p.H_kv + kvh) * D;
+      // Rows sit H_kv * D floats apart, so a thread storing its own row would touch a separate
+      // sector per lane. The rows go through shared memory instead (K, V and the ring are idle once
+      // acc_final has fired: dV in the K and V buffers, dK in the ring), 16-byte chunks
+      // XOR-swizzled by row, and each warp then writes its own 32 rows with kCh lanes per row.
+      constexpr int kCh = D / 4;  // 16-byte chunks per fp32 row
+      float4 *stg = reinterpret_cast<float4 *>(hh == 0 ? smem + C::kOffFixA : sRing);
       const uint32_t col = hh == 0 ? C::kColAcc0 : C::kColAcc1;
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tg::tmem_ld_32x32b_x32(lane_addr + col + c0, v);
         tg::tmem_ld_wait();
-        if (kj < seq_len) {
-          float4 *dst = reinterpret_cast<float4 *>(out + c0);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            dst[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                 __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-        }
+        for (int u = 0; u < 8; ++u)
+          stg[k * kCh + ((c0 / 4 + u) ^ (k & (kCh - 1)))] =
+              make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                          __uint_as_float(v[4 * u + 3]));
+      }
+      __syncwarp();
+      float *out0 = hh == 0 ? p.dV : p.dK;
+      const int cl = lane % kCh;
+#pragma unroll 8
+      for (int rr = 0; rr < 32; rr += 32 / kCh) {
+        const int kt = wq * 32 + rr + lane / kCh;  // key row within the tile
+        const float4 v = stg[kt * kCh + (cl ^ (kt & (kCh - 1)))];
+        if (k0 + kt < seq_len)
+          reinterpret_cast<float4 *>(out0 + (static_cast<size_t>(seq_start + k0 + kt) * p.H_kv + kvh) * D)[cl] = v;
       }
     } else {
       *vabort = 1;
@@ -825,18 +838,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xFFFFFFFFu, tg::mbar_wait(acc_final, 0, vabort, p.wait_limit));
     if (ok) {
       tg::tc_fence_after();
-      float *out = p.dQ + (static_cast<size_t>(seq_start + qi) * p.H_q + h) * D + hh * (D / 2);
+      // The same staging as the dK / dV pass (Q and dO are idle once acc_final has fired: warp
+      // group 0's half rows go to the Q buffer, group 1's to the dO buffer).
+      constexpr int kCh = D / 8;  // 16-byte chunks per half row
+      float4 *stg = reinterpret_cast<float4 *>(hh == 0 ? sQ : smem + C::kOffFixB);
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t v[32];
         tg::tmem_ld_32x32b_x32(lane_addr + C::kColAcc0 + hh * (D / 2) + c0, v);
         tg::tmem_ld_wait();
-        if (qi < seq_len) {
-          float4 *dst = reinterpret_cast<float4 *>(out + c0);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            dst[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                 __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-        }
+        for (int u = 0; u < 8; ++u)
+          stg[r * kCh + ((c0 / 4 + u) ^ (r & (kCh - 1)))] =
+              make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                          __uint_as_float(v[4 * u + 3]));
+      }
+      __syncwarp();
+      const int cl = lane % kCh;
+#pragma unroll 4
+      for (int rr = 0; rr < 32; rr += 32 / kCh) {
+        const int rt = wq * 32 + rr + lane / kCh;  // query row within the tile
+        const float4 v = stg[rt * kCh + (cl ^ (rt & (kCh - 1)))];
+        if (q0 + rt < seq_len)
+          reinterpret_cast<float4 *>(p.dQ + (static_cast<size_t>(seq_start + q0 + rt) * p.H_q + h) * D + hh * (D / 2))[cl] =
+              v;
       }
     } else {
       *vabort = 1;
