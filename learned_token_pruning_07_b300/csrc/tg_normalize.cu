@@ -63,33 +63,79 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   const int hi = start + min(n, (rank + 1) * chunk);
   const int H = GHP == 1 ? 1 : p.H_g;
 
-  float sq[GHP];
-#pragma unroll
-  for (int c = 0; c < GHP; ++c) sq[c] = 0.0f;
+  // GHP = 1: thread t walks rows t, t + kThreads, ... GHP > 1: thread t owns head c = t % GHP of rows
+  // t / GHP, t / GHP + kRows, ..., so a warp reads contiguous (row, head) elements and every
+  // thread keeps the sum of one head. Either way each sum runs over its rows in index order, then
+  // a shuffle tree per warp, then the warps in order.
+  constexpr int kRows = kThreads / GHP;  // rows per step of the CTA
+  constexpr int kU = 4;                  // rows per thread whose loads are issued together
+  const int c_own = tid % GHP;           // GHP > 1: this thread's head
+  float sq = 0.0f;  // this thread's sum of squares (of its one head)
   int cnt = 0;
-  for (int j = lo + tid; j < hi; j += kThreads) {
-    if (p.mask == nullptr || p.mask[j] == 0) {
+  if constexpr (GHP == 1) {
+    // kU rows per step with every load issued first, so their round trips overlap
+    int j = lo + tid;
+    for (; j + (kU - 1) * kThreads < hi; j += kU * kThreads) {
+      uint8_t m[kU];
+      float v[kU];
 #pragma unroll
-      for (int c = 0; c < GHP; ++c) {
-        if (c < H) {
-          const float v = p.s[static_cast<size_t>(j) * H + c];
-          sq[c] = fmaf(v, v, sq[c]);
-        }
+      for (int u = 0; u < kU; ++u) {
+        m[u] = p.mask != nullptr ? p.mask[j + u * kThreads] : uint8_t(0);
+        v[u] = p.s[j + u * kThreads];
       }
-      ++cnt;
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (m[u] == 0) {
+          sq = fmaf(v[u], v[u], sq);
+          ++cnt;
+        }
     }
-  }
+    for (; j < hi; j += kThreads)
+      if (p.mask == nullptr || p.mask[j] == 0) {
+        const float v = p.s[j];
+        sq = fmaf(v, v, sq);
+        ++cnt;
+      }
+  } else {
+    int j = lo + tid / GHP;
+    for (; j + (kU - 1) * kRows < hi; j += kU * kRows) {
+      uint8_t m[kU];
+      float v[kU];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+      for (int u = 0; u < kU; ++u) {
+        const int jj = j + u * kRows;
+        m[u] = p.mask != nullptr ? p.mask[jj] : uint8_t(0);
+        v[u] = c_own < H ? p.s[static_cast<size_t>(jj) * H + c_own] : 0.0f;
+      }
 #pragma unroll
-    for (int c = 0; c < GHP; ++c) sq[c] += __shfl_xor_sync(0xFFFFFFFFu, sq[c], o);
-    cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+      for (int u = 0; u < kU; ++u)
+        if (m[u] == 0) {
+          sq = fmaf(v[u], v[u], sq);
+          cnt += c_own == 0;
+        }
+    }
+    for (; j < hi; j += kRows)
+      if (p.mask == nullptr || p.mask[j] == 0) {
+        const float v = c_own < H ? p.s[static_cast<size_t>(j) * H + c_own] : 0.0f;
+        sq = fmaf(v, v, sq);
+        cnt += c_own == 0;
+      }
   }
-  if (lane == 0) {
+  if constexpr (GHP == 1) {
 #pragma unroll
-    for (int c = 0; c < GHP; ++c) warp_sq[warp][c] = sq[c];
-    warp_n[warp] = cnt;
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+      cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    }
+  } else {
+    // lanes of the same head: xor over the lane bits above the head bits
+#pragma unroll
+    for (int o = 16; o >= GHP; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
   }
+  if (lane == 0) warp_n[warp] = cnt;
+  if (lane < GHP) warp_sq[warp][lane] = sq;
   __syncthreads();
   if (tid < GHP) {
     float t = 0.0f;
@@ -114,19 +160,53 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     inv[tid] = n_doc > 0 ? 1.0f / sqrtf(total / static_cast<float>(n_doc) + p.eps) : 0.0f;
   }
   __syncthreads();
-  for (int j = lo + tid; j < hi; j += kThreads) {
-    const bool keep_always = p.mask != nullptr && p.mask[j] != 0;
-    float sum = 0.0f;
+  if constexpr (GHP == 1) {
+    int jw = lo + tid;
+    for (; jw + (kU - 1) * kThreads < hi; jw += kU * kThreads) {
+      uint8_t m[kU];
+      float v[kU];
 #pragma unroll
-    for (int c = 0; c < GHP; ++c) {
-      if (c < H) {
-        const size_t e = static_cast<size_t>(j) * H + c;
-        const float v = keep_always ? 0.0f : p.s[e] * inv[c];
-        p.b_out[e] = v;
-        sum += v;
+      for (int u = 0; u < kU; ++u) {
+        m[u] = p.mask != nullptr ? p.mask[jw + u * kThreads] : uint8_t(0);
+        v[u] = p.s[jw + u * kThreads];
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) p.b_out[jw + u * kThreads] = m[u] != 0 ? 0.0f : v[u] * inv[0];
+    }
+    for (; jw < hi; jw += kThreads) {
+      const bool keep_always = p.mask != nullptr && p.mask[jw] != 0;
+      p.b_out[jw] = keep_always ? 0.0f : p.s[jw] * inv[0];
+    }
+  } else {
+    // the GHP consecutive lanes of a row also form its head mean (a shuffle tree over them); every
+    // lane of a warp runs the same number of steps, since the shuffles are warp-wide, and rows past
+    // the chunk are skipped inside; kU rows per step with their loads issued first
+    const float inv_c = c_own < H ? inv[c_own] : 0.0f;
+    const int j_first = lo + tid / GHP;
+    const int steps = (hi - lo + kRows - 1) / kRows;
+    for (int k = 0; k < steps; k += kU) {
+      uint8_t m[kU];
+      float sv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int jj = j_first + (k + u) * kRows;
+        const bool in = k + u < steps && jj < hi;
+        m[u] = (in && p.mask != nullptr) ? p.mask[jj] : uint8_t(0);
+        sv[u] = (in && c_own < H) ? p.s[static_cast<size_t>(jj) * H + c_own] : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (k + u >= steps) break;  // uniform across the CTA
+        const int jj = j_first + (k + u) * kRows;
+        const bool in = jj < hi;
+        const float v = m[u] != 0 ? 0.0f : sv[u] * inv_c;
+        if (in && c_own < H) p.b_out[static_cast<size_t>(jj) * H + c_own] = v;
+        float sum = v;
+#pragma unroll
+        for (int o = 1; o < GHP; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (in && p.b_sel != nullptr && c_own == 0) p.b_sel[jj] = sum / static_cast<float>(H);
       }
     }
-    if (GHP > 1 && p.b_sel != nullptr) p.b_sel[j] = sum / static_cast<float>(H);
   }
   cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
 }
