@@ -134,6 +134,7 @@ struct SelShared {
   int4 xch;                 // this CTA's counts: keys > T, keys == T, instruction rows
   int32_t m_b;              // the sequence's end offset in the kept list
   int32_t prev_cnt[kMaxB];  // instruction rows of each earlier sequence inside this chunk
+  int32_t cus[kMaxB + 1];   // cu_seqlens of the earlier sequences (for the searches of that count)
 };
 
 // Block-wide sum of one int per thread (valid in every thread).
@@ -223,17 +224,50 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (p.mask != nullptr && b > 0) {
+    for (int i = tid; i <= b; i += kThreads) sh.cus[i] = p.cu_seqlens[i];
+    __syncthreads();
+    // largest sequence index in [0, b) starting at or before row j
+    auto count_row = [&](int j) {
+      int lo_b = 0, hi_b = b;
+      while (hi_b - lo_b > 1) {
+        const int mid = (lo_b + hi_b) >> 1;
+        if (sh.cus[mid] <= j) lo_b = mid; else hi_b = mid;
+      }
+      atomicAdd(&sh.prev_cnt[lo_b], 1);
+    };
     const int share = (start + kCluster - 1) / kCluster;
     const int a0 = min(start, rank * share), a1 = min(start, (rank + 1) * share);
-    for (int j = a0 + tid; j < a1; j += kThreads) {
-      if (p.mask[j]) {
-        int lo_b = 0, hi_b = b;  // largest sequence index in [0, b) starting at or before j
-        while (hi_b - lo_b > 1) {
-          const int mid = (lo_b + hi_b) >> 1;
-          if (p.cu_seqlens[mid] <= j) lo_b = mid; else hi_b = mid;
-        }
-        atomicAdd(&sh.prev_cnt[lo_b], 1);
+    // whole 4-byte words of the mask in [w0, w1) (mask is 4-byte aligned when p.vec), four words
+    // in flight per thread; the bytes before and after them one at a time
+    const int w0 = p.vec ? min(a1, (a0 + 3) & ~3) : a1;
+    const int w1 = p.vec ? max(w0, a1 & ~3) : a1;
+    for (int j = a0 + tid; j < w0; j += kThreads)
+      if (p.mask[j]) count_row(j);
+    for (int j = w1 + tid; j < a1; j += kThreads)
+      if (p.mask[j]) count_row(j);
+    const uchar4 *m4 = reinterpret_cast<const uchar4 *>(p.mask);
+    const int v0 = w0 >> 2, v1 = w1 >> 2;
+    int v = v0 + tid;
+    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+      uchar4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = m4[v + u * kThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = 4 * (v + u * kThreads);
+        if (q[u].x) count_row(j);
+        if (q[u].y) count_row(j + 1);
+        if (q[u].z) count_row(j + 2);
+        if (q[u].w) count_row(j + 3);
       }
+    }
+    for (; v < v1; v += kThreads) {
+      const uchar4 q = m4[v];
+      const int j = 4 * v;
+      if (q.x) count_row(j);
+      if (q.y) count_row(j + 1);
+      if (q.z) count_row(j + 2);
+      if (q.w) count_row(j + 3);
     }
   }
 
